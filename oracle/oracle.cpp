@@ -1,0 +1,200 @@
+// Plain CPU oracle for the frequency-ranked trimmed drafter head.
+//
+// TEST INFRASTRUCTURE ONLY.  Nothing under frequency_ranked_drafter_gb300/
+// links, loads or calls this file; only tests/, __graft_entry__.smoke() and
+// the cpu_baseline / reference leg of bench.py may do so.  It shares no code,
+// header, table or helper with the CUDA library.
+//
+// Every function is the plain definition of one step, written for a reader
+// who checks it against the pages by eye: single-threaded, no blocking, no
+// fusion, exact integer arithmetic and fp64 for everything that is floating
+// point.  Sources (page title, then section):
+//   [VT]  "VocabTrim: Memory-Efficient Vocabulary Pruning for Speculative
+//         Decoding" (skill page, English and Japanese copies), Implementation
+//         Steps 1-4.
+//   [FR]  "FR-Spec: Accelerating Large-Vocabulary Language Models via
+//         Frequency-Ranked Speculative Sampling" (ACL 2025 paper notes),
+//         Method > Key design "frequency-ranked vocabulary compression".
+//
+// Readings where the pages are silent (each one also listed in the design
+// notes of the repository):
+//   * selection ties: count descending, then lower token id first (the pages
+//     sort a dict by count only, which leaves ties in first-seen order);
+//   * ids never seen are candidates with count 0, so the kept list always has
+//     exactly V_high entries;
+//   * ids outside [0, V) are not counted; they are reported separately and do
+//     not enter the coverage denominator;
+//   * top-k ties: larger logit first, then lower full-vocabulary id.
+//
+// Build: g++ -O2 -std=c++17 -shared -fPIC oracle.cpp -o liboracle.so
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <unordered_map>
+#include <vector>
+
+namespace {
+
+// bf16 is the upper half of an IEEE binary32; widening to double is exact.
+double bf16_to_double(uint16_t bits) {
+  uint32_t u = static_cast<uint32_t>(bits) << 16;
+  float f;
+  std::memcpy(&f, &u, sizeof f);
+  return static_cast<double>(f);
+}
+
+}  // namespace
+
+extern "C" {
+
+// Histogram of a token stream.  [VT] Step 1 counts each id into a dict,
+// token_counts[id] = token_counts.get(id, 0) + 1; [FR] counts corpus tokens.
+// counts[V] is OVERWRITTEN with the dict densified over 0..V-1.
+// *n_invalid receives the number of ids outside [0, V).
+int oracle_count_tokens(const int32_t* tokens, int64_t n, int32_t V,
+                        uint64_t* counts, uint64_t* n_invalid) {
+  if (V <= 0 || n < 0 || counts == nullptr) return 1;
+  std::unordered_map<int32_t, uint64_t> token_counts;
+  uint64_t invalid = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    int32_t id = tokens[i];
+    if (id < 0 || id >= V) {
+      ++invalid;
+      continue;
+    }
+    token_counts[id] += 1;
+  }
+  for (int32_t id = 0; id < V; ++id) counts[id] = 0;
+  for (const auto& kv : token_counts) counts[kv.first] = kv.second;
+  if (n_invalid) *n_invalid = invalid;
+  return 0;
+}
+
+// Vocabulary selection and the two index maps.  [VT] Step 2: sort by count
+// descending, keep the first target_vocab_size entries; the trimmed index of
+// an id is its position in that sorted list (full_to_trimmed /
+// trimmed_to_full); coverage = selected_count / total_count.
+// Outputs: t2f[V_high], f2t[V] (-1 for dropped ids), *kept, *total, and
+// *coverage = kept / total as one IEEE double division (NaN when total = 0).
+int oracle_select_vocab(const uint64_t* counts, int32_t V, int32_t V_high,
+                        int32_t* t2f, int32_t* f2t, uint64_t* kept,
+                        uint64_t* total, double* coverage) {
+  if (V <= 0 || V_high <= 0 || V_high > V) return 1;
+  struct Entry {
+    uint64_t count;
+    int32_t id;
+  };
+  std::vector<Entry> items;
+  items.reserve(V);
+  for (int32_t id = 0; id < V; ++id) items.push_back({counts[id], id});
+  std::sort(items.begin(), items.end(), [](const Entry& a, const Entry& b) {
+    if (a.count != b.count) return a.count > b.count;  // more frequent first
+    return a.id < b.id;                                // tie: lower id first
+  });
+  for (int32_t id = 0; id < V; ++id) f2t[id] = -1;
+  uint64_t selected_count = 0;
+  for (int32_t i = 0; i < V_high; ++i) {
+    t2f[i] = items[i].id;
+    f2t[items[i].id] = i;
+    selected_count += items[i].count;
+  }
+  uint64_t total_count = 0;
+  for (int32_t id = 0; id < V; ++id) total_count += counts[id];
+  if (kept) *kept = selected_count;
+  if (total) *total = total_count;
+  if (coverage)
+    *coverage = static_cast<double>(selected_count) /
+                static_cast<double>(total_count);
+  return 0;
+}
+
+// LM-head reconstruction.  [VT] Step 3: trimmed_weight =
+// original_weight[selected_indices, :], weight stored [vocab, hidden].
+// A row whose index is outside [0, V) is written as zeros (return value 2).
+int oracle_gather_rows(const uint16_t* W, int64_t V, int32_t d,
+                       const int32_t* t2f, int32_t V_high, uint16_t* W_high) {
+  int rc = 0;
+  for (int32_t i = 0; i < V_high; ++i) {
+    int64_t src = t2f[i];
+    uint16_t* dst = W_high + static_cast<int64_t>(i) * d;
+    if (src < 0 || src >= V) {
+      std::memset(dst, 0, sizeof(uint16_t) * d);
+      rc = 2;
+      continue;
+    }
+    std::memcpy(dst, W + src * d, sizeof(uint16_t) * d);
+  }
+  return rc;
+}
+
+// Trimmed projection.  [FR] Key design: the draft LM head projects onto the
+// V_high kept rows only (weight d x 128k -> d x 32k); [VT] Step 4 runs the
+// reconstructed Linear.  logits[m][i] = sum_j H[m][j] * W_high[i][j], every
+// product exact in double, summed in j order.  H rows are ldh elements apart.
+int oracle_head_logits(const uint16_t* H, int32_t M, int32_t d, int64_t ldh,
+                       const uint16_t* W_high, int32_t V_high,
+                       double* logits) {
+  for (int32_t m = 0; m < M; ++m) {
+    const uint16_t* h = H + static_cast<int64_t>(m) * ldh;
+    for (int32_t i = 0; i < V_high; ++i) {
+      const uint16_t* w = W_high + static_cast<int64_t>(i) * d;
+      double acc = 0.0;
+      for (int32_t j = 0; j < d; ++j)
+        acc += bf16_to_double(h[j]) * bf16_to_double(w[j]);
+      logits[static_cast<int64_t>(m) * V_high + i] = acc;
+    }
+  }
+  return 0;
+}
+
+// One draft step of the trimmed head for M hidden states.
+//   logits   : as oracle_head_logits;
+//   softmax  : over the V_high trimmed logits only ([VT] Step 4
+//              trimmed_probs = softmax(drafter_logits); [FR] "softmax is
+//              computed on the subset only"), p_i = exp(l_i - max) / sum_j
+//              exp(l_j - max) in double;
+//   top-k    : the k largest logits (ties: lower full id first), in
+//              descending order; k = 1 is the greedy argmax;
+//   remap    : trimmed index -> full id through t2f ([VT] Step 4 "REMAP");
+//              t2f == nullptr means the identity (the untrimmed head).
+// Outputs per row m (each nullable): ids[m*k+r], probs[m*k+r],
+// top_logits[m*k+r], trimmed_idx[m*k+r], row_max[m], row_sumexp[m].
+int oracle_draft_head(const uint16_t* H, int32_t M, int32_t d, int64_t ldh,
+                      const uint16_t* W_high, int32_t V_high,
+                      const int32_t* t2f, int32_t k, int32_t* ids,
+                      double* probs, double* top_logits, int32_t* trimmed_idx,
+                      double* row_max, double* row_sumexp) {
+  if (M < 0 || d <= 0 || V_high <= 0 || k <= 0 || k > V_high) return 1;
+  std::vector<double> logits(static_cast<size_t>(V_high));
+  std::vector<int32_t> order(static_cast<size_t>(V_high));
+  for (int32_t m = 0; m < M; ++m) {
+    oracle_head_logits(H + static_cast<int64_t>(m) * ldh, 1, d, ldh, W_high,
+                       V_high, logits.data());
+    double mx = logits[0];
+    for (int32_t i = 1; i < V_high; ++i) mx = std::max(mx, logits[i]);
+    double sumexp = 0.0;
+    for (int32_t i = 0; i < V_high; ++i) sumexp += std::exp(logits[i] - mx);
+
+    auto full_id = [&](int32_t i) { return t2f ? t2f[i] : i; };
+    for (int32_t i = 0; i < V_high; ++i) order[i] = i;
+    std::partial_sort(order.begin(), order.begin() + k, order.end(),
+                      [&](int32_t a, int32_t b) {
+                        if (logits[a] != logits[b]) return logits[a] > logits[b];
+                        return full_id(a) < full_id(b);
+                      });
+    for (int32_t r = 0; r < k; ++r) {
+      const int32_t i = order[r];
+      const int64_t o = static_cast<int64_t>(m) * k + r;
+      if (ids) ids[o] = full_id(i);
+      if (probs) probs[o] = std::exp(logits[i] - mx) / sumexp;
+      if (top_logits) top_logits[o] = logits[i];
+      if (trimmed_idx) trimmed_idx[o] = i;
+    }
+    if (row_max) row_max[m] = mx;
+    if (row_sumexp) row_sumexp[m] = sumexp;
+  }
+  return 0;
+}
+
+}  // extern "C"
