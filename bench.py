@@ -1,0 +1,488 @@
+"""Benchmark of the frequency-ranked trimmed drafter head on GB300.
+
+Headline workload: the Llama-3-8B-shaped draft head, d = 4096, full
+vocabulary V = 128256, V_high = 32768 kept rows, M = 1 hidden state (greedy
+draft step), top-1 plus top-k = 10 probabilities.  One step = one call of
+the whole runtime head (projection over the kept rows, softmax over them,
+top-k, remap to full ids) = one kernel launch.
+
+Printed (rank 0, one JSON line): calls/s over all GPUs, the roofline of the
+head kernel against the measured HBM copy bandwidth, the same call end to
+end from pinned host memory, the untrimmed V = 128256 head beside it, the
+offline build at 1e9 tokens (histogram + selection, and the row gather),
+SM clocks sampled during the timed region, and the CPU oracle timed on a
+bounded sample as a baseline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Inputs are seeded and synthetic (weights ~ N(0, 0.02), hidden states
+~ N(0, 1), Zipf(1.1) token streams); every input is resident in HBM before
+the timed region; each call streams a W_high copy of 268 MB, larger than
+L2, and three copies rotate so no call finds its rows in L2.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("trimmed-head calls/s at d=4096 V_high=32k M=1; "
+          "achieved HBM GB/s vs peak")
+WORKLOAD = "llama3-8b drafter head d=4096 V=128256 V_high=32768 M=1 top-k=10"
+HEAD_KERNEL_SRC = os.path.join(ROOT, "frequency_ranked_drafter_gb300", "csrc",
+                               "head_gemv.cu")
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles",
+                               "head_gemv_llama8b_m1_traffic.txt")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-build-bench", action="store_true",
+                    help="skip the 1e9-token build measurement")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------ environment
+
+def dist_init():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle samples while the timed work runs."""
+
+    QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index_or_bus: str):
+        self.target = device_index_or_bus
+        self.proc = None
+        self.lines: list[str] = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50", "-i",
+                 self.target], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self._t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def smi_target(torch, dev) -> str:
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        return "%08x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id,
+                                     p.pci_device_id)
+    except AttributeError:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        return vis.split(",")[dev.index] if vis else str(dev.index)
+
+
+def committed_traffic():
+    """dram bytes per launch of the head kernel from the committed ncu
+    summary, if that summary was taken on the current kernel source."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            kv = dict(line.split(":", 1) for line in f if ":" in line)
+        src_hash = hashlib.sha256(open(HEAD_KERNEL_SRC, "rb").read()).hexdigest()
+        if kv.get("kernel_source_sha256", "").strip() != src_hash:
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------ timing
+
+def time_graph(torch, fn, steps: int, warmup: int, chunk: int = 100,
+               sampler=None):
+    """Capture `chunk` calls of fn(i) in a CUDA graph; run `warmup` calls,
+    then exactly `steps` timed calls.  Returns seconds for the timed part."""
+    stream = torch.cuda.current_stream()
+    chunk = max(1, min(chunk, steps))
+    graphs = {}
+
+    def graph_of(n):
+        if n not in graphs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for i in range(n):
+                    fn(i)
+            graphs[n] = g
+        return graphs[n]
+
+    for i in range(min(warmup, 3)):
+        fn(i)  # eager warm-up first: one-time attribute calls, caches
+    torch.cuda.synchronize()
+    graph_of(chunk)  # capture every graph the timed loop replays up front
+    if steps % chunk:
+        graph_of(steps % chunk)
+    left = max(0, warmup - 3)
+    while left > 0:
+        n = min(chunk, left)
+        graph_of(n).replay()
+        left -= n
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(
+        enable_timing=True)
+    start.record(stream)
+    left = steps
+    while left > 0:
+        n = min(chunk, left)
+        graph_of(n).replay()
+        left -= n
+    end.record(stream)
+    end.synchronize()
+    clocks = sampler.stop() if sampler else None
+    return start.elapsed_time(end) / 1e3, clocks
+
+
+def time_events(torch, fn, reps: int, warmup: int = 2):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(
+            enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        b.synchronize()
+        ts.append(a.elapsed_time(b) / 1e3)
+    return statistics.median(ts)
+
+
+# -------------------------------------------------------------- reference
+
+def oracle_head_rate(d, V_high, k, budget_s, seed=1002):
+    """The CPU oracle on a bounded sample of the head workload: a slice of
+    the kept rows per step, scaled to calls/s."""
+    import numpy as np
+    import torch
+    import oracle
+    import synth
+    rows = min(V_high, 2048)
+    W = synth.bf16_bits(synth.normal_bf16((rows, d), 0.02, seed))
+    H = synth.bf16_bits(synth.normal_bf16((1, d), 1.0, seed + 1))
+    t2f = np.arange(rows, dtype=np.int32)
+    oracle.draft_head(H, W, t2f, k)  # load / warm
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle.draft_head(H, W, t2f, k)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    per_row_s = el / (n * rows)
+    return 1.0 / (per_row_s * V_high), n * rows, el
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    # each of W warm-up + K steps is one oracle slice; keep the run ~2 min
+    budget = max(5.0, min(120.0, 0.5 * (args.steps + args.warmup)))
+    rate, rows, el = oracle_head_rate(4096, 32768, 10, budget)
+    sample = (f"{rows} kept rows of the d=4096 head in {el:.1f} s "
+              f"(fp64 dot products, exact softmax, sorted top-k), scaled to "
+              f"32768 rows per call")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": rate,
+        "unit": "calls/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 / rate,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": "bounded, see cpu_baseline"},
+        "cpu_baseline": {"value": rate, "unit": "calls/s", "cores": 1,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": rate, "unit": "calls/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# -------------------------------------------------------------------- ours
+
+def run_ours(args, world, rank, local):
+    import torch
+    import frequency_ranked_drafter_gb300 as vt
+    import synth
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    vt.load()
+    cfg = synth.LLAMA8B_HEAD
+    d, V, V_high, M, k = cfg.d, cfg.V, cfg.V_high, cfg.M, cfg.k
+    peak, peak_kind = measured_peaks()
+
+    # ---- inputs (resident before any timing)
+    W = synth.normal_bf16((V, d), 0.02, seed=cfg.seed, device=dev)
+    t2f = synth.expected_rank_ids(V, V_high, cfg.seed).to(dev)
+    n_copies = 3
+    W_highs = [vt.gather_rows(W, t2f) for _ in range(n_copies)]
+    H = synth.normal_bf16((M, d), 1.0, seed=cfg.seed + 1, device=dev)
+    ids = torch.empty(M, k, dtype=torch.int32, device=dev)
+    probs = torch.empty(M, k, dtype=torch.float32, device=dev)
+    ws = torch.zeros(vt.workspace_bytes("head", M=M, k=k), dtype=torch.uint8,
+                     device=dev)
+    torch.cuda.synchronize()
+
+    def head_step(i):
+        vt.draft_head(H, W_highs[i % n_copies], t2f, k, out_ids=ids,
+                      out_probs=probs, ws=ws)
+
+    sampler = ClockSampler(smi_target(torch, dev))
+    barrier(world)
+    torch.cuda.synchronize()
+    secs, clocks = time_graph(torch, head_step, args.steps, args.warmup,
+                              sampler=sampler)
+    torch.cuda.synchronize()
+    barrier(world)
+    secs = max_over_ranks(secs, world)
+    per_call = secs / args.steps
+    value = world * args.steps / secs
+    alg_bytes = V_high * d * 2 + M * d * 2 + M * k * 8
+    achieved = alg_bytes / per_call / 1e9
+
+    # ---- end to end: pinned host H in, ids/probs out, synchronised
+    H_host = H.cpu().pin_memory()
+    H_dev = torch.empty_like(H)
+    ids_h = torch.empty(M, k, dtype=torch.int32, pin_memory=True)
+    probs_h = torch.empty(M, k, dtype=torch.float32, pin_memory=True)
+    e2e_steps = min(args.steps, 2000)
+    for i in range(20):
+        vt.draft_head_host(H_host, W_highs[i % n_copies], t2f, k, H_dev=H_dev,
+                           ids_host=ids_h, probs_host=probs_h)
+    barrier(world)
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        vt.draft_head_host(H_host, W_highs[i % n_copies], t2f, k, H_dev=H_dev,
+                           ids_host=ids_h, probs_host=probs_h)
+    e2e_secs = max_over_ranks(time.perf_counter() - t0, world)
+    e2e_value = world * e2e_steps / e2e_secs
+
+    # ---- the untrimmed head (V = 128256, identity map) beside it
+    full_steps = min(args.steps, 5000)
+
+    def full_step(i):
+        vt.draft_head(H, W, None, k, out_ids=ids, out_probs=probs, ws=ws)
+
+    full_secs, _ = time_graph(torch, full_step, full_steps,
+                              max(3, args.warmup // 4))
+    full_per_call = max_over_ranks(full_secs, world) / full_steps
+    full_bytes = V * d * 2 + M * d * 2 + M * k * 8
+
+    out = {
+        "metric": METRIC, "value": value, "unit": "calls/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": per_call * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": WORKLOAD, "d": d, "V": V, "V_high": V_high, "M": M,
+            "k": k, "accumulate": "fp32",
+            "l2": f"inputs larger than L2: {n_copies} rotating W_high copies "
+                  f"of {V_high * d * 2 / 1e6:.0f} MB each",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+            "timing": "CUDA graph replay of 100-call chunks, CUDA events "
+                      "around the timed region",
+        },
+        "us_per_call": per_call * 1e6,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak,
+                     "peak_kind": peak_kind,
+                     "traffic": committed_traffic(),
+                     "alg_bytes_per_launch": alg_bytes,
+                     "kernel": "head_gemv_kernel<1,16,1>"},
+        "e2e": {"value": e2e_value, "unit": "calls/s",
+                "h2d_bytes_per_step": M * d * 2,
+                "d2h_bytes_per_step": M * k * 8,
+                "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "full_vocab": {
+            "V": V, "us_per_call": full_per_call * 1e6,
+            "calls_per_s": 1.0 / full_per_call,
+            "achieved_gbs": full_bytes / full_per_call / 1e9,
+            "frac": full_bytes / full_per_call / 1e9 / peak,
+            "trim_speedup": full_per_call / per_call,
+            "bound_speedup": full_bytes / alg_bytes,
+        },
+    }
+    del W_highs
+
+    if not args.no_build_bench:
+        out["build"] = bench_build(torch, vt, synth, dev, W, peak, world)
+
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, rows, el = oracle_head_rate(d, V_high, k, budget_s=15.0)
+        out["cpu_baseline"] = {
+            "value": rate, "unit": "calls/s", "cores": 1, "kind": "oracle",
+            "sample": f"{rows} kept rows of the d=4096 head in {el:.1f} s on "
+                      f"one host core, scaled to {V_high} rows per call"}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def bench_build(torch, vt, synth, dev, W, peak, world):
+    """1e9-token histogram + selection, and the 32768-row gather."""
+    cfg = synth.SCALE_BUILD
+    tokens = synth.zipf_tokens(cfg.n_tokens, cfg.V, cfg.s, cfg.seed, device=dev)
+    counts = torch.zeros(cfg.V, dtype=torch.uint32, device=dev)
+    n_inv = torch.zeros(1, dtype=torch.int64, device=dev)
+    ws_c = torch.empty(vt.workspace_bytes("count", V=cfg.V), dtype=torch.uint8,
+                       device=dev)
+    ws_s = torch.empty(vt.workspace_bytes("select", V=cfg.V), dtype=torch.uint8,
+                       device=dev)
+    t2f = torch.empty(cfg.V_high, dtype=torch.int32, device=dev)
+    f2t = torch.empty(cfg.V, dtype=torch.int32, device=dev)
+    sums = torch.empty(2, dtype=torch.int64, device=dev)
+
+    def count_only():
+        counts.zero_()
+        vt.count_tokens(tokens, cfg.V, counts=counts, n_invalid=n_inv, ws=ws_c)
+
+    def select_only():
+        vt.select_vocab(counts, cfg.V_high, ws=ws_s, out=(t2f, f2t, sums))
+
+    def both():
+        count_only()
+        select_only()
+
+    t_count = max_over_ranks(time_events(torch, count_only, 5), world)
+    t_select = max_over_ranks(time_events(torch, select_only, 20), world)
+    t_both = max_over_ranks(time_events(torch, both, 5), world)
+    cov = vt.coverage(sums)
+    tok_bytes = cfg.n_tokens * 4
+    del tokens
+    W_high = torch.empty(cfg.V_high, cfg.d, dtype=torch.bfloat16, device=dev)
+    t_gather = max_over_ranks(
+        time_events(torch, lambda: vt.gather_rows(W, t2f, out=W_high), 10),
+        world)
+    g_bytes = 2 * cfg.V_high * cfg.d * 2
+    hs_bytes = tok_bytes + cfg.V * 4 * 2
+    return {
+        "workload": "1e9 Zipf(1.1) int32 tokens, V=128256, V_high=32768, "
+                    "gather of 32768 x 4096 bf16 rows",
+        "histogram_ms": t_count * 1e3,
+        "select_ms": t_select * 1e3,
+        "histogram_select_ms": t_both * 1e3,
+        "tokens_per_s": world * cfg.n_tokens / t_both,
+        "histogram_select_gbs": hs_bytes / t_both / 1e9,
+        "histogram_select_frac": hs_bytes / t_both / 1e9 / peak,
+        "histogram_gbs": tok_bytes / t_count / 1e9,
+        "coverage": cov,
+        "gather_us": t_gather * 1e6,
+        "gather_gbs": g_bytes / t_gather / 1e9,
+        "gather_frac": g_bytes / t_gather / 1e9 / peak,
+    }
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_init()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,280 @@
+"""GB300-native frequency-ranked trimmed drafter head (VocabTrim / FR-Spec).
+
+A thin ctypes binding over the C ABI of ``include/vt.h``.  Every step of the
+path runs in the library's CUDA kernels; this module only checks tensor
+types, allocates outputs and workspaces with PyTorch, and passes device
+pointers and the current CUDA stream.  There is no CPU fallback: if the
+library is missing or a call fails, an exception is raised.
+
+Functions (same names as the C ABI without the ``vt_`` prefix):
+  count_tokens(tokens, V)            -> (counts uint32[V], n_invalid)
+  select_vocab(counts, V_high)       -> (t2f, f2t, sums)   sums = [kept, total]
+  gather_rows(W, t2f)                -> W_high
+  draft_head(H, W_high, t2f, k)      -> (ids int32[M,k], probs f32[M,k])
+and the conveniences build_vocab(...) and coverage(sums).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+__all__ = ["VTError", "load", "library_path", "count_tokens", "select_vocab",
+           "gather_rows", "draft_head", "draft_head_host", "build_vocab",
+           "coverage", "Workspace", "workspace_bytes"]
+
+VT_OK = 0
+_STATUS = {0: "VT_OK", 1: "VT_ERR_INVALID_ARG", 2: "VT_ERR_CUDA",
+           3: "VT_ERR_UNSUPPORTED", 4: "VT_ERR_WORKSPACE", 5: "VT_ERR_TIMEOUT"}
+
+
+class VTError(RuntimeError):
+    def __init__(self, fn: str, status: int, why: str):
+        super().__init__(f"{fn}: {_STATUS.get(status, status)}: {why}")
+        self.status = status
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(build_if_missing: bool = True):
+    """Load (building first if needed) the CUDA library; raises if absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if not os.path.exists(path) or not _build.up_to_date():
+            if not build_if_missing:
+                raise RuntimeError(f"CUDA library not built: {path}")
+            _build.build()
+        lib = ctypes.CDLL(path)
+        p, i32, i64, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
+                           ctypes.c_size_t)
+        sig = {
+            "vt_status_string": ([ctypes.c_int], ctypes.c_char_p),
+            "vt_last_error": ([], ctypes.c_char_p),
+            "vt_version": ([], ctypes.c_int),
+            "vt_count_tokens_workspace_size": ([i32], sz),
+            "vt_count_tokens": ([p, i64, i32, p, p, p, sz, p], ctypes.c_int),
+            "vt_select_vocab_workspace_size": ([i32], sz),
+            "vt_select_vocab": ([p, i32, i32, p, p, p, p, sz, p], ctypes.c_int),
+            "vt_gather_rows": ([p, i64, i32, p, i32, p, p, p], ctypes.c_int),
+            "vt_draft_head_workspace_size": ([i32, i32], sz),
+            "vt_draft_head": ([p, i32, i32, i64, p, i32, p, i32, p, p, p, p,
+                               sz, p], ctypes.c_int),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+        return lib
+
+
+def _check(fn: str, status: int):
+    if status != VT_OK:
+        why = load().vt_last_error().decode(errors="replace")
+        raise VTError(fn, status, why)
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(device: torch.device):
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _cuda(t: torch.Tensor, name: str, dtype: torch.dtype):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+class Workspace:
+    """Per-device, per-stream scratch buffers, grown on demand.
+
+    The draft-head workspace must start zero-filled; the kernels leave it
+    zero-filled again, so it is allocated with zeros once and reused.
+    """
+
+    def __init__(self):
+        self._bufs: dict = {}
+
+    def get(self, kind: str, nbytes: int, device: torch.device,
+            zeroed: bool) -> torch.Tensor:
+        key = (kind, device.index, _stream(device))
+        buf = self._bufs.get(key)
+        if buf is None or buf.numel() < nbytes:
+            alloc = torch.zeros if zeroed else torch.empty
+            buf = alloc(max(nbytes, 256), dtype=torch.uint8, device=device)
+            self._bufs[key] = buf
+        return buf
+
+
+_ws = Workspace()
+
+
+def workspace_bytes(op: str, V: int = 0, M: int = 1, k: int = 1) -> int:
+    """Workspace size of op "count" (V), "select" (V) or "head" (M, k)."""
+    lib = load()
+    if op == "count":
+        return lib.vt_count_tokens_workspace_size(V)
+    if op == "select":
+        return lib.vt_select_vocab_workspace_size(V)
+    if op == "head":
+        return lib.vt_draft_head_workspace_size(M, k)
+    raise ValueError(op)
+
+
+def count_tokens(tokens: torch.Tensor, V: int, counts: torch.Tensor | None = None,
+                 n_invalid: torch.Tensor | None = None,
+                 ws: torch.Tensor | None = None):
+    """Histogram of int32 ``tokens`` over ids 0..V-1 (accumulates into
+    ``counts`` if given).  Returns (counts uint32[V], n_invalid int64[1])."""
+    _cuda(tokens, "tokens", torch.int32)
+    dev = tokens.device
+    if counts is None:
+        counts = torch.zeros(V, dtype=torch.uint32, device=dev)
+    _cuda(counts, "counts", torch.uint32)
+    if n_invalid is None:
+        n_invalid = torch.zeros(1, dtype=torch.int64, device=dev)
+    _cuda(n_invalid, "n_invalid", torch.int64)
+    lib = load()
+    nbytes = lib.vt_count_tokens_workspace_size(V)
+    if ws is None:
+        ws = _ws.get("count", nbytes, dev, zeroed=False)
+    _check("vt_count_tokens", lib.vt_count_tokens(
+        _ptr(tokens), tokens.numel(), V, _ptr(counts), _ptr(n_invalid),
+        _ptr(ws), ws.numel(), _stream(dev)))
+    return counts, n_invalid
+
+
+def select_vocab(counts: torch.Tensor, V_high: int,
+                 ws: torch.Tensor | None = None, out: tuple | None = None):
+    """Top-V_high ids by count (ties: lower id).  Returns (t2f int32[V_high],
+    f2t int32[V] with -1 for dropped ids, sums int64[2] = [kept, total])."""
+    _cuda(counts, "counts", torch.uint32)
+    dev = counts.device
+    V = counts.numel()
+    if out is None:
+        t2f = torch.empty(V_high, dtype=torch.int32, device=dev)
+        f2t = torch.empty(V, dtype=torch.int32, device=dev)
+        sums = torch.empty(2, dtype=torch.int64, device=dev)
+    else:
+        t2f, f2t, sums = out
+    lib = load()
+    nbytes = lib.vt_select_vocab_workspace_size(V)
+    if ws is None:
+        ws = _ws.get("select", nbytes, dev, zeroed=False)
+    _check("vt_select_vocab", lib.vt_select_vocab(
+        _ptr(counts), V, V_high, _ptr(t2f), _ptr(f2t), _ptr(sums), _ptr(ws),
+        ws.numel(), _stream(dev)))
+    return t2f, f2t, sums
+
+
+def coverage(sums: torch.Tensor) -> float:
+    """kept / total from the sums of select_vocab (synchronises)."""
+    kept, total = (int(x) for x in sums.cpu().tolist())
+    return float("nan") if total == 0 else kept / total
+
+
+def gather_rows(W: torch.Tensor, t2f: torch.Tensor,
+                out: torch.Tensor | None = None,
+                n_invalid: torch.Tensor | None = None) -> torch.Tensor:
+    """W_high[i] = W[t2f[i]] for a bf16 [V, d] weight."""
+    _cuda(W, "W", torch.bfloat16)
+    _cuda(t2f, "t2f", torch.int32)
+    V, d = W.shape
+    if out is None:
+        out = torch.empty(t2f.numel(), d, dtype=torch.bfloat16, device=W.device)
+    _cuda(out, "out", torch.bfloat16)
+    if n_invalid is not None:
+        _cuda(n_invalid, "n_invalid", torch.int64)
+    _check("vt_gather_rows", load().vt_gather_rows(
+        _ptr(W), V, d, _ptr(t2f), t2f.numel(), _ptr(out), _ptr(n_invalid),
+        _stream(W.device)))
+    return out
+
+
+def draft_head(H: torch.Tensor, W_high: torch.Tensor, t2f: torch.Tensor | None,
+               k: int, out_ids: torch.Tensor | None = None,
+               out_probs: torch.Tensor | None = None,
+               out_logits: torch.Tensor | None = None,
+               ws: torch.Tensor | None = None):
+    """One draft step: top-k full-vocabulary ids and softmax probabilities
+    over the V_high kept rows for each of the M hidden states in ``H``."""
+    _cuda(W_high, "W_high", torch.bfloat16)
+    if not (isinstance(H, torch.Tensor) and H.is_cuda and H.dtype == torch.bfloat16
+            and H.dim() == 2 and H.stride(1) == 1):
+        raise TypeError("H must be a CUDA bf16 [M, d] tensor with unit column stride")
+    M, d = H.shape
+    V_high = W_high.shape[0]
+    dev = W_high.device
+    if t2f is not None:
+        _cuda(t2f, "t2f", torch.int32)
+    if out_ids is None:
+        out_ids = torch.empty(M, k, dtype=torch.int32, device=dev)
+    if out_probs is None:
+        out_probs = torch.empty(M, k, dtype=torch.float32, device=dev)
+    _cuda(out_ids, "out_ids", torch.int32)
+    _cuda(out_probs, "out_probs", torch.float32)
+    if out_logits is not None:
+        _cuda(out_logits, "out_logits", torch.float32)
+    lib = load()
+    nbytes = lib.vt_draft_head_workspace_size(M, k)
+    if ws is None:
+        ws = _ws.get("head", nbytes, dev, zeroed=True)
+    _check("vt_draft_head", lib.vt_draft_head(
+        _ptr(H), M, d, H.stride(0), _ptr(W_high), V_high, _ptr(t2f), k,
+        _ptr(out_ids), _ptr(out_probs), _ptr(out_logits), _ptr(ws), ws.numel(),
+        _stream(dev)))
+    return out_ids, out_probs
+
+
+def draft_head_host(H_host: torch.Tensor, W_high: torch.Tensor,
+                    t2f: torch.Tensor | None, k: int,
+                    H_dev: torch.Tensor | None = None,
+                    ids_host: torch.Tensor | None = None,
+                    probs_host: torch.Tensor | None = None):
+    """End-to-end call from host memory: copies H (pinned host) to the
+    device, runs draft_head, copies ids/probs back, and synchronises."""
+    dev = W_high.device
+    if H_dev is None:
+        H_dev = torch.empty(H_host.shape, dtype=torch.bfloat16, device=dev)
+    H_dev.copy_(H_host, non_blocking=True)
+    ids, probs = draft_head(H_dev, W_high, t2f, k)
+    if ids_host is None:
+        ids_host = torch.empty(ids.shape, dtype=torch.int32, pin_memory=True)
+    if probs_host is None:
+        probs_host = torch.empty(probs.shape, dtype=torch.float32, pin_memory=True)
+    ids_host.copy_(ids, non_blocking=True)
+    probs_host.copy_(probs, non_blocking=True)
+    torch.cuda.current_stream(dev).synchronize()
+    return ids_host, probs_host
+
+
+def build_vocab(tokens: torch.Tensor, V: int, V_high: int,
+                W: torch.Tensor | None = None):
+    """The offline build in one call: histogram, selection, maps and (if
+    ``W`` is given) the gathered W_high.  Returns a dict of device tensors."""
+    counts, n_invalid = count_tokens(tokens, V)
+    t2f, f2t, sums = select_vocab(counts, V_high)
+    out = dict(counts=counts, n_invalid=n_invalid, t2f=t2f, f2t=f2t, sums=sums)
+    if W is not None:
+        out["W_high"] = gather_rows(W, t2f)
+    return out

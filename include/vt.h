@@ -1,0 +1,169 @@
+/*
+ * vt.h — C ABI of the frequency-ranked trimmed drafter head (GB300, sm_103a).
+ *
+ * The library implements the data-parallel hot path of vocabulary trimming
+ * for speculative-decoding drafters:
+ *   offline build : token histogram -> top-V_high selection -> the two index
+ *                   maps -> row gather of the kept lm_head rows;
+ *   runtime head  : logits over the V_high kept rows only, fused with the
+ *                   softmax over that subset, top-k, and the remap of the
+ *                   chosen trimmed indices back to full-vocabulary ids.
+ *
+ * Sources (page title, then section):
+ *   [VT] "VocabTrim: Memory-Efficient Vocabulary Pruning for Speculative
+ *        Decoding" (skill page, English and Japanese copies), Architecture
+ *        Overview and Implementation Steps 1-4.
+ *   [FR] "FR-Spec: Accelerating Large-Vocabulary Language Models via
+ *        Frequency-Ranked Speculative Sampling" (ACL 2025 paper notes),
+ *        Method > Key design "frequency-ranked vocabulary compression".
+ *
+ * Conventions for every call
+ *   - Pointers marked (device) must be device memory of the current CUDA
+ *     device (or managed memory); (host) pointers are host memory.
+ *   - bf16 tensors are passed as `const uint16_t*` holding the bf16 bit
+ *     patterns; all matrices are row-major and densely packed.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
+ *     call is asynchronous and stream-ordered; none synchronises, allocates
+ *     or frees.  The caller owns every buffer.
+ *   - Argument errors are detected on the host before anything is launched
+ *     and are returned synchronously (VT_ERR_INVALID_ARG, VT_ERR_WORKSPACE,
+ *     VT_ERR_UNSUPPORTED); nothing is written in that case.  A failed launch
+ *     returns VT_ERR_CUDA.  vt_last_error() gives a one-line reason for the
+ *     latest non-OK status returned on the calling thread.
+ *   - Data errors inside buffers (ids outside the vocabulary) never trap:
+ *     they are counted into an optional device counter and skipped.
+ *   - Calls that take a workspace (`ws`) need one of at least the size the
+ *     matching *_workspace_size function returns, 256-byte aligned.  Calls
+ *     running concurrently (other streams) need distinct workspaces.
+ */
+#ifndef VT_H_
+#define VT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum vt_status {
+  VT_OK = 0,
+  VT_ERR_INVALID_ARG = 1, /* null pointer, bad size or alignment */
+  VT_ERR_CUDA = 2,        /* a CUDA runtime call or launch failed */
+  VT_ERR_UNSUPPORTED = 3, /* valid but outside what this build supports */
+  VT_ERR_WORKSPACE = 4,   /* workspace missing, too small or misaligned */
+  VT_ERR_TIMEOUT = 5      /* reserved: a bounded device wait gave up */
+} vt_status;
+
+/* Static string naming a status code. */
+const char* vt_status_string(int status);
+
+/* One-line reason for the latest non-OK status returned on this thread
+ * ("" if none).  The pointer stays valid until the next call on the thread. */
+const char* vt_last_error(void);
+
+/* Library ABI version (major * 100 + minor). */
+int vt_version(void);
+
+/* ------------------------------------------------------------------------
+ * vt_count_tokens — token-frequency histogram.
+ * [VT] Step 1 counts every sampled id into a dict; [FR] Key design counts
+ * corpus tokens.  Here the stream is counted into a dense array.
+ *
+ *   tokens    (device) int32[n], any values; 16-byte aligned.
+ *   n         number of tokens, 0 <= n < 2^40.
+ *   V         vocabulary size, 1 <= V <= 2^30.
+ *   counts    (device) uint32[V]; ACCUMULATED INTO (counts[id] += hits), so
+ *             a long stream may be counted in pieces.  Zero it before the
+ *             first piece.  Arithmetic is modulo 2^32 per id.
+ *   n_invalid (device, nullable) uint64[1]; accumulated: the number of
+ *             tokens outside [0, V), which are not counted anywhere.
+ *   ws        (device) workspace of vt_count_tokens_workspace_size(V) bytes.
+ * ------------------------------------------------------------------------ */
+size_t vt_count_tokens_workspace_size(int32_t V);
+vt_status vt_count_tokens(const int32_t* tokens, int64_t n, int32_t V,
+                          uint32_t* counts, uint64_t* n_invalid, void* ws,
+                          size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * vt_select_vocab — top-V_high selection and the two index maps.
+ * [VT] Step 2: sort ids by count descending, keep the first V_high; the
+ * trimmed index of an id is its rank; coverage = selected / total.
+ * Tie rule (the pages leave it to dict order): lower id first, so the
+ * result is unique.  Ids with count 0 take part, so exactly V_high ids are
+ * always kept.
+ *
+ *   counts    (device) uint32[V].
+ *   V_high    1 <= V_high <= V.
+ *   t2f       (device) int32[V_high]: trimmed index -> full id, rank order
+ *             (t2f[0] is the most frequent id).
+ *   f2t       (device) int32[V]: full id -> trimmed index, -1 if dropped.
+ *   sums      (device) uint64[2]: OVERWRITTEN with {kept, total}: the sum of
+ *             the kept ids' counts and of all counts.  Coverage is
+ *             (double)kept / (double)total, computed by the caller after
+ *             the stream is synchronised (NaN when total == 0).
+ *   ws        (device) workspace of vt_select_vocab_workspace_size(V) bytes.
+ * ------------------------------------------------------------------------ */
+size_t vt_select_vocab_workspace_size(int32_t V);
+vt_status vt_select_vocab(const uint32_t* counts, int32_t V, int32_t V_high,
+                          int32_t* t2f, int32_t* f2t, uint64_t* sums,
+                          void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * vt_gather_rows — reconstruct the trimmed lm_head.
+ * [VT] Step 3: W_high = W[trimmed_to_full, :], W stored [vocab, hidden].
+ * A bit-exact copy of V_high rows of d bf16 values.
+ *
+ *   W         (device) bf16[V, d], 16-byte aligned.
+ *   d         hidden size, d > 0 and d % 8 == 0.
+ *   t2f       (device) int32[V_high].
+ *   W_high    (device) bf16[V_high, d], 16-byte aligned, must not overlap W.
+ *   n_invalid (device, nullable) uint64[1]; accumulated: rows whose t2f
+ *             entry lies outside [0, V); such rows are written as zeros.
+ * ------------------------------------------------------------------------ */
+vt_status vt_gather_rows(const uint16_t* W, int64_t V, int32_t d,
+                         const int32_t* t2f, int32_t V_high, uint16_t* W_high,
+                         uint64_t* n_invalid, void* stream);
+
+/* ------------------------------------------------------------------------
+ * vt_draft_head — one draft step of the trimmed head for M hidden states.
+ * [FR] Key design: the draft lm_head projects onto the V_high kept rows only
+ * and the softmax is taken over that subset; [VT] Step 4: softmax of the
+ * drafter logits, then the chosen trimmed index is mapped back to the full
+ * vocabulary through trimmed_to_full before verification.
+ *
+ *   logit[m][i] = sum_j H[m][j] * W_high[i][j]   (bf16 inputs, fp32 sums)
+ *   p[m][i]     = exp(logit[m][i] - max_i) / sum_i exp(logit[m][i] - max_i)
+ *   out         = the k largest logits of row m, in descending order;
+ *                 out_ids = t2f[i] (full-vocabulary ids), out_probs = p.
+ *   Equal logits are ordered by lower trimmed index.
+ *
+ *   H         (device) bf16, M rows of d values, row stride ldh elements
+ *             (ldh >= d, ldh % 8 == 0), 16-byte aligned.
+ *   M         number of hidden states (draft-tree nodes), 1 <= M <= 256.
+ *   d         hidden size, d % 8 == 0, 8 <= d <= 16384.
+ *   W_high    (device) bf16[V_high, d], 16-byte aligned.
+ *   V_high    1 <= V_high < 2^31.
+ *   t2f       (device, nullable) int32[V_high]; NULL means the identity,
+ *             i.e. the untrimmed head over a full vocabulary of V_high rows.
+ *   k         1 <= k <= 32 and k <= V_high.  k = 1 is the greedy argmax.
+ *   out_ids   (device) int32[M, k].
+ *   out_probs (device) float[M, k].
+ *   out_logits(device, nullable) float[M, V_high]: every trimmed logit, for
+ *             verification; costs an extra write of M*V_high*4 bytes.
+ *   ws        (device) workspace of vt_draft_head_workspace_size(M, k)
+ *             bytes.  It must be zero-filled once before its first use;
+ *             every call leaves it zero-filled again.
+ * ------------------------------------------------------------------------ */
+size_t vt_draft_head_workspace_size(int32_t M, int32_t k);
+vt_status vt_draft_head(const uint16_t* H, int32_t M, int32_t d, int64_t ldh,
+                        const uint16_t* W_high, int32_t V_high,
+                        const int32_t* t2f, int32_t k, int32_t* out_ids,
+                        float* out_probs, float* out_logits, void* ws,
+                        size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VT_H_ */

@@ -1,0 +1,73 @@
+"""Helpers shared by the GPU parity tests (comparison rules, host copies)."""
+import numpy as np
+import pytest
+import torch
+
+# Tolerances of the trimmed head (bf16 inputs, fp32 accumulation):
+#   |logit_gpu - logit_oracle| <= 1e-3 * (1 + |logit_oracle|)
+#   |prob_gpu  - prob_oracle|  <= 1e-4
+LOGIT_RTOL = 1e-3
+PROB_ATOL = 1e-4
+
+
+def need_cuda():
+    assert torch.cuda.is_available(), "GPU test run without a CUDA device"
+    return torch.device("cuda", torch.cuda.current_device())
+
+
+def u32_host(t: torch.Tensor) -> np.ndarray:
+    assert t.dtype == torch.uint32
+    return t.view(torch.int32).cpu().numpy().view(np.uint32)
+
+
+def bits_host(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def logit_tol(ref):
+    return LOGIT_RTOL * (1.0 + np.abs(ref))
+
+
+def check_logits(gpu_logits: np.ndarray, ref: np.ndarray):
+    bad = np.abs(gpu_logits.astype(np.float64) - ref) > logit_tol(ref)
+    assert not bad.any(), (
+        f"{bad.sum()} logits out of tolerance; worst at "
+        f"{np.unravel_index(np.argmax(np.abs(gpu_logits - ref)), ref.shape)}")
+
+
+def check_topk(ids, probs, ref_logits, t2f, oracle_res, k):
+    """GPU top-k of each row against the oracle.
+
+    ``ref_logits`` [M, V_high] are the oracle's fp64 trimmed logits.  Rank r
+    of the GPU's answer must name a kept row whose oracle logit is within the
+    logit tolerance of the oracle's r-th best logit (so ids differ from the
+    oracle's only where oracle scores are that close), ids must be distinct,
+    and each probability must match the oracle's probability of the same id.
+    """
+    M = ref_logits.shape[0]
+    V_high = ref_logits.shape[1]
+    if t2f is None:
+        full_to_row = {i: i for i in range(V_high)} if V_high < 4096 else None
+    else:
+        full_to_row = {int(f): i for i, f in enumerate(t2f)}
+    exact = 0
+    for m in range(M):
+        o_ids = oracle_res["ids"][m]
+        o_log = oracle_res["logits"][m]
+        mx = oracle_res["row_max"][m]
+        se = oracle_res["row_sumexp"][m]
+        g = ids[m].tolist()
+        assert len(set(g)) == k, f"row {m}: repeated ids {g}"
+        for r in range(k):
+            gid = int(g[r])
+            row = gid if full_to_row is None else full_to_row.get(gid)
+            assert row is not None and 0 <= row < V_high, f"row {m}: id {gid} not kept"
+            lv = ref_logits[m, row]
+            assert abs(lv - o_log[r]) <= logit_tol(o_log[r]), (
+                f"row {m} rank {r}: gpu id {gid} (logit {lv}) vs oracle id "
+                f"{o_ids[r]} (logit {o_log[r]})")
+            p_ref = np.exp(lv - mx) / se
+            assert abs(float(probs[m, r]) - p_ref) <= PROB_ATOL, (
+                f"row {m} rank {r}: prob {probs[m, r]} vs {p_ref}")
+        exact += int(list(g) == o_ids.tolist())
+    return exact

@@ -1,0 +1,109 @@
+"""The C ABI without a GPU: the library builds and loads, exports every
+function include/vt.h declares, and rejects bad arguments on the host
+before touching the device (nothing here makes a CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import frequency_ranked_drafter_gb300 as vt
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "vt.h")
+
+OK, INVALID, CUDA, UNSUPPORTED, WORKSPACE = 0, 1, 2, 3, 4
+FAKE = 1 << 20  # a 256-byte aligned non-null address never dereferenced
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(vt_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return vt.load()
+
+
+def test_header_declares_the_four_calls():
+    names = declared_functions()
+    for fn in ("vt_count_tokens", "vt_select_vocab", "vt_gather_rows",
+               "vt_draft_head"):
+        assert fn in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(vt.library_path())
+    missing = [n for n in declared_functions() if not hasattr(raw, n)]
+    assert not missing, missing
+
+
+def test_status_strings_and_version(lib):
+    assert lib.vt_status_string(0) == b"VT_OK"
+    assert lib.vt_status_string(1) == b"VT_ERR_INVALID_ARG"
+    assert lib.vt_status_string(99) == b"VT_ERR_UNKNOWN"
+    assert lib.vt_version() >= 100
+
+
+def test_workspace_sizes(lib):
+    assert lib.vt_count_tokens_workspace_size(0) == 0
+    assert lib.vt_count_tokens_workspace_size(128256) >= 128256
+    assert lib.vt_select_vocab_workspace_size(128256) >= 16 * 128256
+    assert lib.vt_draft_head_workspace_size(1, 10) > 256
+    assert (lib.vt_draft_head_workspace_size(64, 10)
+            > lib.vt_draft_head_workspace_size(1, 10))
+
+
+def test_draft_head_rejects_bad_arguments(lib):
+    ws_ok = lib.vt_draft_head_workspace_size(1, 10)
+
+    def call(H=FAKE, M=1, d=4096, ldh=4096, W=FAKE, V_high=32768, t2f=None,
+             k=10, ids=FAKE, probs=FAKE, logits=None, ws=FAKE, ws_bytes=ws_ok):
+        return lib.vt_draft_head(H, M, d, ldh, W, V_high, t2f, k, ids, probs,
+                                 logits, ws, ws_bytes, None)
+
+    assert call(H=None) == INVALID
+    assert call(M=0) == INVALID
+    assert call(M=257) == INVALID
+    assert call(d=4095, ldh=4095) == INVALID
+    assert call(ldh=4000) == INVALID
+    assert call(k=0) == INVALID
+    assert call(k=33) == INVALID
+    assert call(V_high=5, k=6) == INVALID
+    assert call(H=FAKE + 2) == INVALID  # misaligned
+    assert call(ws=None) == WORKSPACE
+    assert call(ws_bytes=ws_ok - 1) == WORKSPACE
+    assert call(ws=FAKE + 16) == WORKSPACE
+    assert b"workspace" in lib.vt_last_error()
+
+
+def test_count_select_gather_reject_bad_arguments(lib):
+    wsc = lib.vt_count_tokens_workspace_size(100)
+    assert lib.vt_count_tokens(FAKE, 10, 0, FAKE, None, FAKE, wsc, None) == INVALID
+    assert lib.vt_count_tokens(FAKE, -1, 100, FAKE, None, FAKE, wsc, None) == INVALID
+    assert lib.vt_count_tokens(FAKE + 4, 10, 100, FAKE, None, FAKE, wsc, None) == INVALID
+    assert lib.vt_count_tokens(FAKE, 10, 100, FAKE, None, FAKE, wsc - 1, None) == WORKSPACE
+    # n == 0 is a valid no-op that never touches the device
+    assert lib.vt_count_tokens(None, 0, 100, FAKE, None, FAKE, wsc, None) == OK
+
+    wss = lib.vt_select_vocab_workspace_size(100)
+    assert lib.vt_select_vocab(FAKE, 100, 0, FAKE, FAKE, FAKE, FAKE, wss, None) == INVALID
+    assert lib.vt_select_vocab(FAKE, 100, 101, FAKE, FAKE, FAKE, FAKE, wss, None) == INVALID
+    assert lib.vt_select_vocab(FAKE, 100, 10, FAKE, FAKE, FAKE, FAKE, wss - 1, None) == WORKSPACE
+    assert lib.vt_select_vocab(FAKE, 1 << 25, 10, FAKE, FAKE, FAKE, FAKE, 1 << 40, None) == UNSUPPORTED
+
+    assert lib.vt_gather_rows(FAKE, 100, 12, FAKE, 10, FAKE * 4, None, None) == INVALID
+    assert lib.vt_gather_rows(FAKE, 100, 16, None, 10, FAKE * 4, None, None) == INVALID
+    # overlapping output
+    assert lib.vt_gather_rows(FAKE, 100, 16, FAKE, 10, FAKE + 32, None, None) == INVALID
+
+
+def test_python_binding_refuses_cpu_tensors():
+    import torch
+    with pytest.raises(TypeError):
+        vt.count_tokens(torch.zeros(8, dtype=torch.int32), 4)
+    with pytest.raises(TypeError):
+        vt.draft_head(torch.zeros(1, 8, dtype=torch.bfloat16),
+                      torch.zeros(4, 8, dtype=torch.bfloat16), None, 1)

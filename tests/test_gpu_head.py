@@ -1,0 +1,148 @@
+"""GPU parity of the trimmed draft head against the CPU oracle, through the
+C ABI: every logit (when requested) within 1e-3 * (1 + |l|), probabilities
+within 1e-4, top-k ids equal to the oracle's except where oracle logits are
+closer than that tolerance, at small sizes spanning many CTAs and ragged
+tails and at the full Llama-3-8B / Qwen-2-7B / Llama-3.2-1B head shapes."""
+import numpy as np
+import pytest
+import torch
+
+import frequency_ranked_drafter_gb300 as vt
+import oracle
+import synth
+from gpu_util import bits_host, check_logits, check_topk, need_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+def run_case(d, V_high, M, k, seed, hs=1.0, ws=0.02, use_t2f=True,
+             V=None, ldh=None, want_logits=True, check_rows=None):
+    dev = need_cuda()
+    V = V or max(V_high, 2 * V_high)
+    W_high = synth.normal_bf16((V_high, d), ws, seed=seed, device=dev)
+    Hfull = synth.normal_bf16((M, ldh or d), hs, seed=seed + 1, device=dev)
+    H = Hfull[:, :d]
+    t2f = None
+    if use_t2f:
+        t2f = synth.rank_permutation(V, seed)[:V_high].to(dev)
+    logits = (torch.empty(M, V_high, dtype=torch.float32, device=dev)
+              if want_logits else None)
+    ids, probs = vt.draft_head(H, W_high, t2f, k, out_logits=logits)
+    torch.cuda.synchronize()
+    rows = list(range(M)) if check_rows is None else check_rows
+    Hh = bits_host(H[rows])
+    Wh = bits_host(W_high)
+    t2f_h = None if t2f is None else t2f.cpu().numpy()
+    ref = oracle.draft_head(Hh, Wh, t2f_h, k)
+    ref_logits = oracle.head_logits(Hh, Wh)
+    if want_logits:
+        check_logits(logits.cpu().numpy()[rows], ref_logits)
+    exact = check_topk(ids.cpu().numpy()[rows], probs.cpu().numpy()[rows],
+                       ref_logits, t2f_h, ref, k)
+    return exact, ids, probs
+
+
+def test_tiny_pipeline_head():
+    """Tiny workload end to end: build W_high with the library, then draft."""
+    dev = need_cuda()
+    cfg, hcfg = synth.TINY_BUILD, synth.TINY_HEAD
+    tokens = synth.zipf_tokens(cfg.n_tokens, cfg.V, cfg.s, cfg.seed).to(dev)
+    W = synth.normal_bf16((cfg.V, cfg.d), 0.02, seed=cfg.seed, device=dev)
+    b = vt.build_vocab(tokens, cfg.V, cfg.V_high, W)
+    H = synth.normal_bf16((1, cfg.d), 1.0, seed=cfg.seed + 1, device=dev)
+    logits = torch.empty(1, cfg.V_high, dtype=torch.float32, device=dev)
+    ids, probs = vt.draft_head(H, b["W_high"], b["t2f"], hcfg.k,
+                               out_logits=logits)
+    Hh, Wh = bits_host(H), bits_host(b["W_high"])
+    t2f_h = b["t2f"].cpu().numpy()
+    ref = oracle.draft_head(Hh, Wh, t2f_h, hcfg.k)
+    ref_logits = oracle.head_logits(Hh, Wh)
+    check_logits(logits.cpu().numpy(), ref_logits)
+    check_topk(ids.cpu().numpy(), probs.cpu().numpy(), ref_logits, t2f_h, ref,
+               hcfg.k)
+
+
+@pytest.mark.parametrize("d,V_high,M,k", [
+    (256, 1024, 1, 8),
+    (264, 3001, 1, 10),     # ragged d (not a multiple of 256) and ragged rows
+    (520, 2047, 2, 5),
+    (1032, 5000, 3, 16),
+    (2048, 4099, 4, 10),
+    (3584, 1500, 1, 32),
+    (4096, 777, 1, 1),      # greedy argmax
+    (8192, 600, 2, 10),     # d above one row block of loads
+    (16384, 300, 1, 3),
+    (4096, 10, 1, 10),      # k = V_high: every row returned
+    (256, 1, 1, 1),         # a single kept row
+])
+def test_head_shapes(d, V_high, M, k):
+    run_case(d, V_high, M, k, seed=d + V_high)
+
+
+def test_head_identity_map_and_strided_H():
+    run_case(1024, 3000, 2, 10, seed=5, use_t2f=False, ldh=1040)
+
+
+def test_head_many_hidden_states_grouped():
+    """M above the GEMV group size: handled four hidden states at a time."""
+    run_case(512, 2000, 9, 10, seed=9)
+
+
+def test_head_large_logits_no_overflow():
+    exact, _, probs = run_case(1024, 4000, 1, 10, seed=11, hs=64.0, ws=1.0)
+    assert torch.isfinite(probs).all()
+
+
+def test_head_uniform_logits_ties():
+    """All logits equal: probabilities are exactly 1/V_high; the GPU orders
+    equal logits by trimmed index, the oracle by full id, so only the
+    probabilities and the validity of ids are compared."""
+    dev = need_cuda()
+    V_high, d, k = 3000, 256, 10
+    W = torch.zeros(V_high, d, dtype=torch.bfloat16, device=dev)
+    H = torch.ones(1, d, dtype=torch.bfloat16, device=dev)
+    t2f = torch.arange(V_high, dtype=torch.int32, device=dev).flip(0).contiguous()
+    ids, probs = vt.draft_head(H, W, t2f, k)
+    torch.testing.assert_close(probs, torch.full_like(probs, 1.0 / V_high),
+                               rtol=1e-5, atol=0)
+    assert sorted(set(ids[0].tolist())) == sorted(ids[0].tolist())
+    # lowest trimmed indices first: t2f[0..k-1]
+    assert ids[0].tolist() == t2f[:k].tolist()
+
+
+def test_head_repeated_calls_identical():
+    """The workspace ticket is re-armed by every call."""
+    dev = need_cuda()
+    W = synth.normal_bf16((20000, 1024), 0.02, seed=1, device=dev)
+    H = synth.normal_bf16((1, 1024), 1.0, seed=2, device=dev)
+    first = vt.draft_head(H, W, None, 10)
+    first = [t.clone() for t in first]
+    for _ in range(5):
+        ids, probs = vt.draft_head(H, W, None, 10)
+        assert torch.equal(ids, first[0]) and torch.equal(probs, first[1])
+
+
+# ------------------------------------------------------- full-size shapes
+
+def test_llama3_8b_trimmed_head_full_size():
+    cfg = synth.LLAMA8B_HEAD
+    run_case(cfg.d, cfg.V_high, cfg.M, cfg.k, seed=cfg.seed, V=cfg.V)
+
+
+def test_llama3_8b_full_vocab_head():
+    cfg = synth.LLAMA8B_HEAD
+    run_case(cfg.d, cfg.V, 1, cfg.k, seed=cfg.seed, use_t2f=False)
+
+
+@pytest.mark.parametrize("shape", [synth.QWEN7B_HEAD, synth.LLAMA1B_HEAD])
+@pytest.mark.parametrize("M", [1, 4])
+def test_qwen_and_llama1b_heads(shape, M):
+    run_case(shape.d, shape.V_high, M, shape.k, seed=shape.seed + M, V=shape.V)
+
+
+def test_tree_draft_m60_sampled_rows():
+    """M = 60 tree nodes at V_high = 32768: every row on the GPU, five
+    sampled rows against the oracle."""
+    cfg = synth.TREE_HEAD
+    run_case(cfg.d, cfg.V_high, cfg.M, cfg.k, seed=cfg.seed, V=cfg.V,
+             want_logits=False, check_rows=[0, 17, 31, 48, 59])
