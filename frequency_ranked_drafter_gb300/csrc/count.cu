@@ -49,30 +49,46 @@ __device__ __noinline__ void settle_wrap(uint32_t old, uint32_t word,
   }
 }
 
-__device__ __forceinline__ void count_token(uint32_t* sm, int32_t t,
-                                            uint32_t lo, uint32_t Vr,
-                                            uint32_t V, bool count_invalid,
-                                            uint32_t* counts_pass,
-                                            uint32_t& invalid) {
-  const uint32_t u = static_cast<uint32_t>(t) - lo;
-  if (u < Vr) {
-    const uint32_t word = u >> 2;
-    const uint32_t sh = (u & 3u) << 3;
-    const uint32_t old = atomicAdd(&sm[word], 1u << sh);
-    if (((old >> sh) & 0xffu) == 0xffu)
-      settle_wrap(old, word, u & 3u, counts_pass, Vr);
-  } else if (count_invalid && static_cast<uint32_t>(t) >= V) {
-    ++invalid;
+// Counts one token whose word / shift are known; returns the old word.
+__device__ __forceinline__ uint32_t smem_hit(uint32_t* sm, uint32_t u) {
+  return atomicAdd(&sm[u >> 2], 1u << ((u & 3u) << 3));
+}
+
+// Eight tokens: all shared-memory atomics are issued back to back, and the
+// (rare) byte wraps are settled afterwards, so the atomics' latencies
+// overlap instead of each one gating a branch.
+__device__ __forceinline__ void count8(uint32_t* sm, const int32_t (&t)[8],
+                                       uint32_t lo, uint32_t Vr, uint32_t V,
+                                       bool ci, uint32_t* counts_pass,
+                                       uint32_t& invalid) {
+  uint32_t old[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t u = static_cast<uint32_t>(t[j]) - lo;
+    old[j] = 0;
+    if (u < Vr) old[j] = smem_hit(sm, u);
+    else if (ci && static_cast<uint32_t>(t[j]) >= V) ++invalid;
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t u = static_cast<uint32_t>(t[j]) - lo;
+    if (u < Vr && ((old[j] >> ((u & 3u) << 3)) & 0xffu) == 0xffu)
+      settle_wrap(old[j], u >> 2, u & 3u, counts_pass, Vr);
   }
 }
 
-__device__ __forceinline__ void count_token4(uint32_t* sm, int4 v, uint32_t lo,
-                                             uint32_t Vr, uint32_t V, bool ci,
-                                             uint32_t* cp, uint32_t& inv) {
-  count_token(sm, v.x, lo, Vr, V, ci, cp, inv);
-  count_token(sm, v.y, lo, Vr, V, ci, cp, inv);
-  count_token(sm, v.z, lo, Vr, V, ci, cp, inv);
-  count_token(sm, v.w, lo, Vr, V, ci, cp, inv);
+__device__ __forceinline__ void count1(uint32_t* sm, int32_t t, uint32_t lo,
+                                       uint32_t Vr, uint32_t V, bool ci,
+                                       uint32_t* counts_pass,
+                                       uint32_t& invalid) {
+  const uint32_t u = static_cast<uint32_t>(t) - lo;
+  if (u < Vr) {
+    const uint32_t old = smem_hit(sm, u);
+    if (((old >> ((u & 3u) << 3)) & 0xffu) == 0xffu)
+      settle_wrap(old, u >> 2, u & 3u, counts_pass, Vr);
+  } else if (ci && static_cast<uint32_t>(t) >= V) {
+    ++invalid;
+  }
 }
 
 __global__ void __launch_bounds__(kCountThreads, 1)
@@ -97,16 +113,21 @@ __global__ void __launch_bounds__(kCountThreads, 1)
     const int4 b = ld_stream_i4(t4 + i + stride);
     const int4 c = ld_stream_i4(t4 + i + 2 * stride);
     const int4 d = ld_stream_i4(t4 + i + 3 * stride);
-    count_token4(sm, a, lo, Vr, V, ci, counts_pass, invalid);
-    count_token4(sm, b, lo, Vr, V, ci, counts_pass, invalid);
-    count_token4(sm, c, lo, Vr, V, ci, counts_pass, invalid);
-    count_token4(sm, d, lo, Vr, V, ci, counts_pass, invalid);
+    const int32_t x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    count8(sm, x, lo, Vr, V, ci, counts_pass, invalid);
+    const int32_t y[8] = {c.x, c.y, c.z, c.w, d.x, d.y, d.z, d.w};
+    count8(sm, y, lo, Vr, V, ci, counts_pass, invalid);
   }
-  for (; i < n4; i += stride)
-    count_token4(sm, ld_stream_i4(t4 + i), lo, Vr, V, ci, counts_pass, invalid);
+  for (; i < n4; i += stride) {
+    const int4 a = ld_stream_i4(t4 + i);
+    count1(sm, a.x, lo, Vr, V, ci, counts_pass, invalid);
+    count1(sm, a.y, lo, Vr, V, ci, counts_pass, invalid);
+    count1(sm, a.z, lo, Vr, V, ci, counts_pass, invalid);
+    count1(sm, a.w, lo, Vr, V, ci, counts_pass, invalid);
+  }
   if (blockIdx.x == 0 && threadIdx.x < (n & 3))
-    count_token(sm, tokens[(n4 << 2) + threadIdx.x], lo, Vr, V, ci,
-                counts_pass, invalid);
+    count1(sm, tokens[(n4 << 2) + threadIdx.x], lo, Vr, V, ci, counts_pass,
+           invalid);
   __syncthreads();
 
   uint32_t* slab = slabs + (size_t)blockIdx.x * words_padded;
@@ -121,36 +142,49 @@ __global__ void __launch_bounds__(kCountThreads, 1)
   }
 }
 
-// counts[lo + 4w + b] += sum over CTAs of byte b of slab word w.  Bytes are
-// summed in two registers of 16-bit lanes (at most 256 * 255 < 2^16).
+// counts[lo + 4w + b] += sum over CTAs of byte b of slab word w.  A CTA
+// handles 32 words; its 8 warps each sum one eighth of the slabs with all
+// loads of a thread issued together, and the eight partial sums are added
+// in shared memory.  Bytes are summed in two registers of 16-bit lanes
+// (at most 256 * 255 < 2^16).
+constexpr int kReduceGroups = 8;
 __global__ void __launch_bounds__(256)
     count_reduce_kernel(const uint32_t* __restrict__ slabs, int G,
                         int words_padded, uint32_t Vr,
                         uint32_t* __restrict__ counts_pass) {
-  const uint32_t w = blockIdx.x * 256 + threadIdx.x;
-  if (w >= (Vr + 3) / 4) return;
+  __shared__ uint32_t part[kReduceGroups][32][2];
+  const int lane = threadIdx.x & 31, grp = threadIdx.x >> 5;
+  const uint32_t w = blockIdx.x * 32 + lane;
+  const uint32_t nwords = (Vr + 3) / 4;
   uint32_t even = 0, odd = 0;  // bytes 0,2 and 1,3 of every slab word
-  int b = 0;
-  for (; b + 8 <= G; b += 8) {
-    uint32_t x[8];
+  if (w < nwords) {
+    constexpr int kPer = kCountMaxCtas / kReduceGroups;  // 32 slabs max
+    uint32_t x[kPer];
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      x[j] = __ldcg(slabs + (size_t)(b + j) * words_padded + w);
+    for (int j = 0; j < kPer; ++j) {
+      const int b = grp + j * kReduceGroups;
+      x[j] = b < G ? __ldcg(slabs + (size_t)b * words_padded + w) : 0u;
+    }
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < kPer; ++j) {
       even += x[j] & 0x00ff00ffu;
       odd += (x[j] >> 8) & 0x00ff00ffu;
     }
   }
-  for (; b < G; ++b) {
-    const uint32_t x = __ldcg(slabs + (size_t)b * words_padded + w);
-    even += x & 0x00ff00ffu;
-    odd += (x >> 8) & 0x00ff00ffu;
-  }
-  const uint32_t s[4] = {even & 0xffffu, odd & 0xffffu, even >> 16, odd >> 16};
+  part[grp][lane][0] = even;
+  part[grp][lane][1] = odd;
+  __syncthreads();
+  if (grp == 0 && w < nwords) {
+    for (int g = 1; g < kReduceGroups; ++g) {
+      even += part[g][lane][0];
+      odd += part[g][lane][1];
+    }
+    const uint32_t s4[4] = {even & 0xffffu, odd & 0xffffu, even >> 16,
+                            odd >> 16};
 #pragma unroll
-  for (int j = 0; j < 4; ++j)
-    if (4 * w + j < Vr) counts_pass[4 * w + j] += s[j];
+    for (int j = 0; j < 4; ++j)
+      if (4 * w + j < Vr) counts_pass[4 * w + j] += s4[j];
+  }
 }
 
 int words_for(uint32_t Vr) { return (int)(((Vr + 3) / 4 + 3) & ~3u); }
@@ -199,7 +233,7 @@ extern "C" vt_status vt_count_tokens(const int32_t* tokens, int64_t n,
         reinterpret_cast<unsigned long long*>(n_invalid), slabs, words);
     vt_status st = launch_status("count_tokens_kernel");
     if (st != VT_OK) return st;
-    const int rb = (int)(((Vr + 3) / 4 + 255) / 256);
+    const int rb = (int)(((Vr + 3) / 4 + 31) / 32);
     count_reduce_kernel<<<rb, 256, 0, s>>>(slabs, G, words, Vr, counts + lo);
     st = launch_status("count_reduce_kernel");
     if (st != VT_OK) return st;

@@ -13,8 +13,7 @@ namespace vt {
 constexpr int kTopKMax = 32;
 constexpr int kHeadMaxCtas = 1024;
 constexpr int kHeadTicketBytes = 256;
-constexpr int kSurvivorCap = 1024;
-constexpr int kStageBytesMax = 160 * 1024;  // staged partials, last CTA
+constexpr int kStageBytesMax = 96 * 1024;  // staged candidates, last CTA
 
 // Each CTA publishes, per hidden state m, `pstride` 32-bit words:
 //   [0] max logit of its rows, [1] sum of exp(logit - max) over its rows,
@@ -34,10 +33,21 @@ struct HeadArgs {
   float* out_logits;   // [M, V_high] or null
   float* part;         // [grid][M][pstride]
   int pstride;
-  unsigned* ticket;
+  unsigned* ticket;      // [0]: CTAs done; [1]: next dynamically dealt row group
 };
 
 inline int head_pstride(int k) { return 2 + 2 * k; }
+
+// Arrival on a grid-wide ticket: atomic increment with acquire-release
+// semantics at gpu scope; returns the previous count.
+__device__ __forceinline__ unsigned ticket_arrive(unsigned* ticket) {
+  unsigned prev;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;"
+               : "=r"(prev)
+               : "l"(ticket)
+               : "memory");
+  return prev;
+}
 
 __device__ __forceinline__ bool key_beats(float v, int i, float v2, int i2) {
   return v > v2 || (v == v2 && i < i2);
@@ -86,94 +96,158 @@ __device__ __forceinline__ void block_best(float& v, int& i, float* sv,
   __syncthreads();
 }
 
-// Merge of all CTAs' partial results, run by the last CTA of a launch.
-// `stage` is shared memory of at least G * pstride words (the caller sizes
-// the launch so that it fits).  For every hidden state m:
-//   global max  Mg = max_b max_b;   Sg = sum_b sumexp_b * exp(max_b - Mg);
-//   threshold   T0 = the best of the CTAs' k-th entries: the global k-th
-//               entry can be no worse, so only entries not beaten by T0 can
-//               be in the global top-k (usually about k of them);
-//   ranks       of those survivors by counting, written out in order.
-// If more than kSurvivorCap entries survive (adversarial inputs), the top-k
-// falls back to k rounds of a block-wide arg-max.
+// Order-preserving image of a float in uint32 (larger float -> larger
+// key; -0 and +0 share one key; -inf -> 0x007fffff, so 0 is below every
+// real value).
+__device__ __forceinline__ unsigned float_key(float f) {
+  unsigned u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Shared-memory scratch of head_final_merge (8 warps).
+struct MergeScratch {
+  float w_val[8 * kTopKMax];  // level-1 winners of each warp
+  int w_idx[8 * kTopKMax];
+  float w_max[8];
+  float w_sum[8];
+};
+
+// Merge of all CTAs' partial results, run by the last CTA of a launch
+// (NT = 256 threads, 8 warps).  For every hidden state m:
+//   Mg = max_b max_b;  Sg = sum_b sumexp_b * exp(max_b - Mg);
+//   level 1: warp w merges lists [w*L, (w+1)*L) (L = ceil(G/8), at most
+//            four lists per lane, their heads in registers) by a k-round
+//            tournament; a round is a warp arg-max done with two redux.sync
+//            (max of the order-preserving logit key, then min of the index
+//            among the lanes holding it), after which the winning list
+//            advances;
+//   level 2: the 8*k level-1 winners are ranked by counting and the k best
+//            written out by k threads at once (remap, exp, divide).
+// All partials are read in one batch of independent loads (one L2 round
+// trip) and the lists staged in shared memory (`stage`, G*k*8 bytes): this
+// part runs on one SM while the others idle.  Its cost does not depend on
+// the data.
 template <int NT>
 __device__ void head_final_merge(const HeadArgs& a, int MR, int G,
-                                 float* stage, float* red_v, int* red_i,
-                                 float2* surv, int* s_cnt) {
-  const int tid = threadIdx.x;
-  const int k = a.k, ps = a.pstride;
-  int* stage_i = reinterpret_cast<int*>(stage);
+                                 float* stage, MergeScratch& sc) {
+  static_assert(NT == 256, "merge layout assumes 8 warps");
+  constexpr int kPer = kHeadMaxCtas / NT;      // CTA summaries per thread
+  constexpr int kBatch = 16;                   // candidates per thread per batch
+  constexpr int kOwn = kHeadMaxCtas / 8 / 32;  // lists per lane (level 1)
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int k = a.k, ps = a.pstride, nc = G * k;
+  float* sv = stage;
+  int* si = reinterpret_cast<int*>(stage + nc);
   for (int m = 0; m < MR; ++m) {
-    for (int t = tid; t < G * ps; t += NT) {
-      const int b = t / ps, o = t % ps;
-      stage[t] = __ldcg(a.part + ((size_t)b * MR + m) * ps + o);
+    auto slot = [&](int b) { return a.part + ((size_t)b * MR + m) * ps; };
+    float bm[kPer], bs[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int b = tid + j * NT;
+      bm[j] = b < G ? __ldcg(slot(b)) : -INFINITY;
+      bs[j] = b < G ? __ldcg(slot(b) + 1) : 0.f;
     }
-    if (tid == 0) *s_cnt = 0;
-    __syncthreads();
-
-    float mg = -INFINITY, t0v = -INFINITY;
-    int t0i = INT_MAX;
-    for (int b = tid; b < G; b += NT) {
-      mg = fmaxf(mg, stage[b * ps]);
-      const float kv = stage[b * ps + 2 + k - 1];
-      const int ki = stage_i[b * ps + 2 + 2 * k - 1];
-      if (key_beats(kv, ki, t0v, t0i)) { t0v = kv; t0i = ki; }
-    }
-    mg = block_max<NT>(mg, red_v);
-    block_best<NT>(t0v, t0i, red_v, red_i);
-    float sg = 0.f;
-    for (int b = tid; b < G; b += NT) {
-      const float s = stage[b * ps + 1];
-      if (s > 0.f) sg += s * __expf(stage[b * ps] - mg);
-    }
-    sg = block_sum<NT>(sg, red_v);
-
-    for (int c = tid; c < G * k; c += NT) {
-      const int b = c / k, j = c % k;
-      const float v = stage[b * ps + 2 + j];
-      const int i = stage_i[b * ps + 2 + k + j];
-      if (i != INT_MAX && !key_beats(t0v, t0i, v, i)) {
-        const int p = atomicAdd(s_cnt, 1);
-        if (p < kSurvivorCap) surv[p] = make_float2(v, __int_as_float(i));
+    for (int base = 0; base < nc; base += NT * kBatch) {
+      float cv[kBatch];
+      int ci[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int c = base + j * NT + tid;
+        if (c < nc) {
+          const int b = c / k, r = c - b * k;
+          cv[j] = __ldcg(slot(b) + 2 + r);
+          ci[j] = __ldcg(reinterpret_cast<const int*>(slot(b)) + 2 + k + r);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int c = base + j * NT + tid;
+        if (c < nc) { sv[c] = cv[j]; si[c] = ci[j]; }
       }
     }
+    float wm = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) wm = fmaxf(wm, bm[j]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(~0u, wm, o));
+    if (lane == 0) sc.w_max[warp] = wm;
+    __syncthreads();  // publishes the stage and the warp maxima
+    float mg = sc.w_max[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) mg = fmaxf(mg, sc.w_max[w]);
+    float ws = 0.f;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j)
+      if (bs[j] > 0.f) ws += bs[j] * __expf(bm[j] - mg);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(~0u, ws, o);
+    if (lane == 0) sc.w_sum[warp] = ws;
+
+    // ---- level 1: per-warp tournament over its lists
+    {
+      const int L = (G + 7) / 8;
+      const int b0 = warp * L, b1 = min(G, b0 + L);
+      int hd[kOwn];
+      float hv[kOwn];
+      int hi[kOwn];
+#pragma unroll
+      for (int o = 0; o < kOwn; ++o) {
+        const int b = b0 + lane + 32 * o;
+        hd[o] = 0;
+        hv[o] = b < b1 ? sv[b * k] : -INFINITY;
+        hi[o] = b < b1 ? si[b * k] : INT_MAX;
+      }
+      float rv = -INFINITY;
+      int ri = INT_MAX;
+      for (int r = 0; r < k; ++r) {
+        float lv = -INFINITY;
+        int li = INT_MAX, lo = 0;
+#pragma unroll
+        for (int o = 0; o < kOwn; ++o)
+          if (hi[o] != INT_MAX && key_beats(hv[o], hi[o], lv, li)) {
+            lv = hv[o]; li = hi[o]; lo = o;
+          }
+        const unsigned lk = li != INT_MAX ? float_key(lv) : 0u;
+        const unsigned wk = __reduce_max_sync(~0u, lk);
+        if (wk == 0u) break;  // this warp's lists are exhausted
+        const int wi = (int)__reduce_min_sync(
+            ~0u, lk == wk ? (unsigned)li : 0xffffffffu);
+        const unsigned owner = __ballot_sync(~0u, lk == wk && li == wi);
+        const int ol = __ffs(owner) - 1;
+        const float wv = __shfl_sync(~0u, lv, ol);
+        if (lane == r) { rv = wv; ri = wi; }
+        if (lane == ol) {  // the winning list advances
+#pragma unroll
+          for (int o = 0; o < kOwn; ++o)
+            if (o == lo) {
+              const int b = b0 + lane + 32 * o;
+              const int h = ++hd[o];
+              hv[o] = h < k ? sv[b * k + h] : -INFINITY;
+              hi[o] = h < k ? si[b * k + h] : INT_MAX;
+            }
+        }
+      }
+      if (lane < k) { sc.w_val[warp * k + lane] = rv; sc.w_idx[warp * k + lane] = ri; }
+    }
     __syncthreads();
-    const int S = *s_cnt;
+
+    // ---- level 2: rank the 8*k level-1 winners, write the k best
+    float sg = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) sg += sc.w_sum[w];
     int32_t* ids = a.out_ids + (size_t)m * k;
     float* probs = a.out_probs + (size_t)m * k;
-    if (S <= kSurvivorCap) {
-      for (int s = tid; s < S; s += NT) {
-        const float v = surv[s].x;
-        const int i = __float_as_int(surv[s].y);
-        int rank = 0;
-        for (int q = 0; q < S; ++q)
-          rank += key_beats(surv[q].x, __float_as_int(surv[q].y), v, i);
-        if (rank < k) {
-          ids[rank] = a.t2f ? a.t2f[i] : i;
-          probs[rank] = expf(v - mg) / sg;
-        }
-      }
-    } else {
-      float pv = INFINITY;
-      int pi = INT_MIN;
-      for (int r = 0; r < k; ++r) {
-        float bv = -INFINITY;
-        int bi = INT_MAX;
-        for (int c = tid; c < G * k; c += NT) {
-          const int b = c / k, j = c % k;
-          const float v = stage[b * ps + 2 + j];
-          const int i = stage_i[b * ps + 2 + k + j];
-          if (i != INT_MAX && key_beats(pv, pi, v, i) &&
-              key_beats(v, i, bv, bi)) { bv = v; bi = i; }
-        }
-        block_best<NT>(bv, bi, red_v, red_i);
-        if (tid == 0) {
-          const bool ok = bi != INT_MAX;
-          ids[r] = !ok ? -1 : (a.t2f ? a.t2f[bi] : bi);
-          probs[r] = ok ? expf(bv - mg) / sg : 0.f;
-        }
-        pv = bv;
-        pi = bi;
+    for (int c = tid; c < 8 * k; c += NT) {
+      const float v = sc.w_val[c];
+      const int i = sc.w_idx[c];
+      if (i == INT_MAX) continue;
+      int rank = 0;
+      for (int q = 0; q < 8 * k; ++q)
+        rank += key_beats(sc.w_val[q], sc.w_idx[q], v, i);
+      if (rank < k) {
+        ids[rank] = a.t2f ? a.t2f[i] : i;
+        probs[rank] = expf(v - mg) / sg;
       }
     }
     __syncthreads();

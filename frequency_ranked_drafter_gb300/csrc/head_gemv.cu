@@ -57,10 +57,8 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
   __shared__ float c_val[MR][kGemvWarps * kTopKMax];
   __shared__ int c_idx[MR][kGemvWarps * kTopKMax];
   __shared__ float w_mx[MR][kGemvWarps], w_se[MR][kGemvWarps];
-  __shared__ float r_val[kGemvWarps];
-  __shared__ int r_idx[kGemvWarps];
-  __shared__ float2 surv[kSurvivorCap];
-  __shared__ int s_cnt, s_last;
+  __shared__ MergeScratch msc;
+  __shared__ int s_last;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int d = a.d, k = a.k;
@@ -92,7 +90,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
   const float4* h4 = reinterpret_cast<const float4*>(hs);
   const int ngroups = (a.V_high + U - 1) / U;
 
-  for (int g = gwarp; g < ngroups; g += gwarps) {
+  auto process_group = [&](int g) {
     const int r0 = g * U;
     float acc[U][MR];
 #pragma unroll
@@ -155,6 +153,25 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
         }
       }
     }
+  };
+
+  // Rows are dealt in groups of U.  Most groups go round-robin over all
+  // warps of the grid; the last ~1/8 are handed out one at a time from a
+  // global counter, so warps that stream faster take more and all warps
+  // finish together.  A warp asks for its next dynamic group one group ahead.
+  const int static_rounds = (ngroups / gwarps) * 7 / 8;
+  const int n_static = static_rounds * gwarps;
+  int g_next = 0;
+  if (lane == 0) g_next = (int)atomicAdd(a.ticket + 1, 1u);
+  for (int it = 0, g = gwarp;; ++it) {
+    if (it < static_rounds) {
+      g = gwarp + it * gwarps;
+    } else {
+      g = n_static + __shfl_sync(~0u, g_next, 0);
+      if (g >= ngroups) break;
+      if (lane == 0) g_next = (int)atomicAdd(a.ticket + 1, 1u);
+    }
+    process_group(g);
   }
 
   // ---- CTA merge: rank counting over the warps' lists.
@@ -199,16 +216,19 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
     part[m * a.pstride + 1] = S_b;
   }
 
-  // ---- last CTA merges every CTA's (max, sumexp, top-k).
-  __threadfence();
+  // ---- last CTA merges every CTA's (max, sumexp, top-k).  The barrier
+  // orders the CTA's partial writes before thread 0's gpu-scope release on
+  // the ticket; the last arrival's acquire (and the barrier after it) makes
+  // every CTA's partials visible to the whole merging CTA.
   __syncthreads();
-  if (tid == 0) s_last = atomicAdd(a.ticket, 1u) == gridDim.x - 1;
+  if (tid == 0) s_last = ticket_arrive(a.ticket) == gridDim.x - 1;
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
-  head_final_merge<kGemvThreads>(a, MR, gridDim.x, hs, r_val, r_idx, surv,
-                                 &s_cnt);
-  if (tid == 0) *a.ticket = 0u;
+  head_final_merge<kGemvThreads>(a, MR, gridDim.x, hs, msc);
+  if (tid == 0) {
+    a.ticket[0] = 0u;
+    a.ticket[1] = 0u;
+  }
 }
 
 template <int MR, int CPL, int U>
@@ -216,18 +236,14 @@ vt_status launch_gemv(const HeadArgs& a, const DeviceInfo& di,
                       cudaStream_t s) {
   auto kern = head_gemv_kernel<MR, CPL, U>;
   const int64_t groups = (a.V_high + U - 1) / U;
-  const int64_t stage_per_cta = (int64_t)a.pstride * sizeof(float);
-  auto smem_for = [&](int64_t G) {
-    return (int)std::max<int64_t>((int64_t)MR * a.d * sizeof(float),
-                                  G * stage_per_cta);
-  };
-  // Aim for two CTAs per SM (the launch bound), fewer if the partials of
-  // that many CTAs would not fit the last CTA's shared memory.
+  // Two CTAs per SM (the launch bound); no more CTAs than warps have rows,
+  // and no more than the last CTA can stage candidates of (G * k * 8 bytes).
   int64_t G = std::min<int64_t>((int64_t)di.num_sms * 2,
                                 (groups + kGemvWarps - 1) / kGemvWarps);
-  G = std::min<int64_t>(G, kStageBytesMax / stage_per_cta);
+  G = std::min<int64_t>(G, kStageBytesMax / (8 * a.k));
   G = std::max<int64_t>(1, std::min<int64_t>(G, kHeadMaxCtas));
-  const int smem = smem_for(G);
+  const int smem = (int)std::max<int64_t>((int64_t)MR * a.d * sizeof(float),
+                                          G * a.k * 8);
   if (smem > di.max_smem_optin)
     return fail(VT_ERR_UNSUPPORTED, "head_gemv: M * d too large for smem");
   if (!allow_max_smem(kern, di)) return VT_ERR_CUDA;

@@ -36,10 +36,17 @@ __global__ void __launch_bounds__(kSelThreads)
   __shared__ uint32_t h[256];
   h[threadIdx.x] = 0;
   __syncthreads();
-  const int begin = blockIdx.x * kSelTile;
-  const int end = min(V, begin + kSelTile);
-  for (int e = begin + threadIdx.x; e < end; e += kSelThreads)
-    atomicAdd(&h[digit_of(keys[e], shift)], 1u);
+  uint32_t key[kSelRounds];
+#pragma unroll
+  for (int r = 0; r < kSelRounds; ++r) {  // all loads first, then counting
+    const int e = blockIdx.x * kSelTile + r * kSelThreads + threadIdx.x;
+    key[r] = e < V ? keys[e] : 0u;
+  }
+#pragma unroll
+  for (int r = 0; r < kSelRounds; ++r) {
+    const int e = blockIdx.x * kSelTile + r * kSelThreads + threadIdx.x;
+    if (e < V) atomicAdd(&h[digit_of(key[r], shift)], 1u);
+  }
   __syncthreads();
   tile_hist[threadIdx.x * T + blockIdx.x] = h[threadIdx.x];
   if (sums_to_zero && blockIdx.x == 0 && threadIdx.x < 2)
@@ -80,12 +87,27 @@ __global__ void __launch_bounds__(kSelThreads)
   __shared__ unsigned long long red[2][kWarps];
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
 
+  // The tile's keys and values, loaded up front (round-major order).
+  uint32_t keyr[kSelRounds];
+  int32_t valr[kSelRounds];
+#pragma unroll
+  for (int r = 0; r < kSelRounds; ++r) {
+    const int e = blockIdx.x * kSelTile + r * kSelThreads + t;
+    keyr[r] = e < V ? keys_in[e] : 0u;
+    valr[r] = e < V ? (vals_in ? vals_in[e] : e) : 0;
+  }
   {  // output offset of digit t for this tile
     uint32_t total = 0, before = 0;
-    for (int j = 0; j < T; ++j) {
-      const uint32_t c = tile_hist[t * T + j];
-      total += c;
-      if (j < (int)blockIdx.x) before += c;
+    for (int j0 = 0; j0 < T; j0 += 8) {
+      uint32_t c[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        c[j] = j0 + j < T ? tile_hist[t * T + j0 + j] : 0u;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        total += c[j];
+        if (j0 + j < (int)blockIdx.x) before += c[j];
+      }
     }
     offs[t] = block_exclusive_scan(total, warp_tot) + before;
   }
@@ -95,11 +117,12 @@ __global__ void __launch_bounds__(kSelThreads)
 
   unsigned long long kept = 0, total = 0;
   const unsigned lt_mask = (1u << lane) - 1u;
+#pragma unroll
   for (int r = 0; r < kSelRounds; ++r) {
     const int e = blockIdx.x * kSelTile + r * kSelThreads + t;
     const bool valid = e < V;
-    const uint32_t key = valid ? keys_in[e] : 0u;
-    const int32_t val = valid ? (vals_in ? vals_in[e] : e) : 0;
+    const uint32_t key = keyr[r];
+    const int32_t val = valr[r];
     const uint32_t dig = valid ? digit_of(key, shift) : 256u;
     const unsigned peers = __match_any_sync(~0u, dig);
     const uint32_t rank = __popc(peers & lt_mask);

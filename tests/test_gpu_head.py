@@ -111,7 +111,10 @@ def test_head_uniform_logits_ties():
 
 
 def test_head_repeated_calls_identical():
-    """The workspace ticket is re-armed by every call."""
+    """The workspace counters are re-armed by every call: repeated calls
+    return the same ids; the probabilities agree to rounding (the last
+    rows are load-balanced dynamically, so the order of the sum of exps
+    may differ between calls)."""
     dev = need_cuda()
     W = synth.normal_bf16((20000, 1024), 0.02, seed=1, device=dev)
     H = synth.normal_bf16((1, 1024), 1.0, seed=2, device=dev)
@@ -119,7 +122,8 @@ def test_head_repeated_calls_identical():
     first = [t.clone() for t in first]
     for _ in range(5):
         ids, probs = vt.draft_head(H, W, None, 10)
-        assert torch.equal(ids, first[0]) and torch.equal(probs, first[1])
+        assert torch.equal(ids, first[0])
+        torch.testing.assert_close(probs, first[1], rtol=1e-6, atol=0)
 
 
 # ------------------------------------------------------- full-size shapes
