@@ -162,6 +162,35 @@ vt_status vt_draft_head(const uint16_t* H, int32_t M, int32_t d, int64_t ldh,
                         float* out_probs, float* out_logits, void* ws,
                         size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------------------------------
+ * vt_draft_head_noalloc — vt_draft_head for callers that cannot allocate.
+ * The pages have no counterpart to this call; it exists for integration.
+ *
+ * Some callers cannot allocate device memory where they run a draft step
+ * (inside a CUDA stream capture that must not gain allocation nodes, on
+ * hosts that forbid allocation after start-up, or as a plugin confined to
+ * another framework's memory pool), so they cannot provide the workspace
+ * vt_draft_head needs.  This call computes exactly what vt_draft_head
+ * computes, with the same arguments minus the workspace, and allocates
+ * nothing: its scratch is one fixed 1 MiB array in device memory that the
+ * library defines and every GPU that loads the library keeps until exit.
+ *
+ *   Limit     the scratch needed, vt_draft_head_workspace_size(min(M, 4), k),
+ *             must fit in 1 MiB (any k <= 32 for M <= 3; k <= 30 for
+ *             M >= 4); larger requests return VT_ERR_UNSUPPORTED.
+ *   Set-up    the first call on each device looks up the array's device
+ *             address and zero-fills its counters with a synchronous
+ *             cudaMemset; make that first call before any stream capture.
+ *   Sharing   all calls on a device share the one array; calls that overlap
+ *             on the GPU (unordered streams) race on it and give wrong
+ *             results.  Calls on one stream are safe.
+ * ------------------------------------------------------------------------ */
+vt_status vt_draft_head_noalloc(const uint16_t* H, int32_t M, int32_t d,
+                                int64_t ldh, const uint16_t* W_high,
+                                int32_t V_high, const int32_t* t2f, int32_t k,
+                                int32_t* out_ids, float* out_probs,
+                                float* out_logits, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
