@@ -30,111 +30,181 @@ namespace {
 constexpr int kCountThreads = 1024;
 constexpr int kCountMaxCtas = 256;               // workspace is sized for this
 constexpr int64_t kTokensPerCta = 1 << 17;       // below this, fewer CTAs
-constexpr int kCountMaxIds = 224 * 1024;         // ids per pass (bytes of smem)
+constexpr int kCountMaxIds = 208 * 1024;         // ids per pass (bytes of smem)
 
+// Byte wraps (and the carries they push into the next byte of the word)
+// are settled in 32-bit counters.  Wraps come from frequent ids, so a small
+// shared-memory table (kCacheSlots direct-mapped slots, tagged with the id,
+// claimed by compare-and-swap) holds those counters for the hot ids and is
+// added to the global counts once at the end; an id whose slot is taken by
+// another id goes to the global counts directly.  This keeps the hottest
+// ids from receiving one global atomic per 256 hits from every CTA.
+constexpr int kCacheSlots = 2048;
+constexpr uint32_t kEmptyTag = 0xffffffffu;
+
+struct WrapCache {
+  uint32_t tag[kCacheSlots];
+  uint32_t cnt[kCacheSlots];
+};
+
+__device__ __forceinline__ void cache_add(WrapCache& wc, uint32_t u,
+                                          uint32_t delta, uint32_t* counts) {
+  const uint32_t slot = u & (kCacheSlots - 1);
+  uint32_t t = wc.tag[slot];
+  if (t == kEmptyTag) {
+    const uint32_t prev = atomicCAS(&wc.tag[slot], kEmptyTag, u);
+    t = prev == kEmptyTag ? u : prev;
+  }
+  if (t == u) atomicAdd(&wc.cnt[slot], delta);
+  else atomicAdd(&counts[u], delta);
+}
+
+// The hit that made byte b0 of shared word `word` wrap (old byte 0xff):
+// +256 for that id; the carry added 1 to the next byte, so -1 for the next
+// id, which may itself have wrapped (+256), and so on along the word.
 __device__ __noinline__ void settle_wrap(uint32_t old, uint32_t word,
                                          uint32_t b0, uint32_t* counts,
-                                         uint32_t Vr) {
+                                         uint32_t Vr, WrapCache& wc) {
   const uint32_t base = word << 2;
-  atomicAdd(&counts[base + b0], 256u);  // byte b0 wrapped once
+  cache_add(wc, base + b0, 256u, counts);
   for (uint32_t b = b0 + 1; b < 4; ++b) {
     if (base + b >= Vr) break;  // padding byte: never counted, never reported
     const uint32_t ob = (old >> (8 * b)) & 0xffu;
     if (ob == 0xffu) {
-      atomicAdd(&counts[base + b], 255u);  // carry in (-1) and a wrap (+256)
+      cache_add(wc, base + b, 255u, counts);  // carry in (-1) and a wrap (+256)
     } else {
-      atomicAdd(&counts[base + b], 0xffffffffu);  // carry in only: -1
+      cache_add(wc, base + b, 0xffffffffu, counts);  // carry in only: -1
       break;
     }
   }
 }
 
-// Counts one token whose word / shift are known; returns the old word.
-__device__ __forceinline__ uint32_t smem_hit(uint32_t* sm, uint32_t u) {
-  return atomicAdd(&sm[u >> 2], 1u << ((u & 3u) << 3));
+// Sixteen tokens of one thread.  The sixteen shared-memory atomics issue
+// back to back (their latencies overlap); a token's byte wrapped if its old
+// value was 0xff, and all sixteen checks fold into one predicate, so the
+// rare wraps (once per 256 hits of an id) cost one branch per 16 tokens.
+// kSingle: the pass covers every id (lo = 0, Vr = V), so "in range" and
+// "valid" are the same test.
+template <bool kSingle>
+__device__ __forceinline__ void count16(uint32_t* sm, const int4 (&v)[4],
+                                        uint32_t lo, uint32_t Vr, uint32_t V,
+                                        uint32_t* counts_pass,
+                                        uint32_t& invalid, WrapCache& wc) {
+  uint32_t t[16], olds[16];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    t[4 * q + 0] = (uint32_t)v[q].x;
+    t[4 * q + 1] = (uint32_t)v[q].y;
+    t[4 * q + 2] = (uint32_t)v[q].z;
+    t[4 * q + 3] = (uint32_t)v[q].w;
+  }
+  uint32_t wraps = 0;  // bit j: token j's byte wrapped
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const uint32_t u = kSingle ? t[j] : t[j] - lo;
+    const bool in = u < Vr;
+    const uint32_t sh = (u << 3) & 24u;
+    olds[j] = 0u;
+    if (in) olds[j] = atomicAdd(&sm[u >> 2], 1u << sh);
+    if (in && ((~olds[j] >> sh) & 0xffu) == 0u) wraps |= 1u << j;
+    if (kSingle) invalid += in ? 0u : 1u;
+    else if (lo == 0) invalid += t[j] >= V ? 1u : 0u;
+  }
+  // A warp sees about two wraps per step of 512 tokens, so this loop runs
+  // in most steps, but only over the wrapped tokens of each thread.
+  while (wraps) {
+    const int j = __ffs(wraps) - 1;
+    wraps &= wraps - 1;
+    uint32_t tj = 0, oj = 0;
+#pragma unroll
+    for (int q = 0; q < 16; ++q)
+      if (q == j) { tj = t[q]; oj = olds[q]; }
+    const uint32_t u = kSingle ? tj : tj - lo;
+    settle_wrap(oj, u >> 2, u & 3u, counts_pass, Vr, wc);
+  }
 }
 
-// Eight tokens: all shared-memory atomics are issued back to back, and the
-// (rare) byte wraps are settled afterwards, so the atomics' latencies
-// overlap instead of each one gating a branch.
-__device__ __forceinline__ void count8(uint32_t* sm, const int32_t (&t)[8],
-                                       uint32_t lo, uint32_t Vr, uint32_t V,
-                                       bool ci, uint32_t* counts_pass,
-                                       uint32_t& invalid) {
-  uint32_t old[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const uint32_t u = static_cast<uint32_t>(t[j]) - lo;
-    old[j] = 0;
-    if (u < Vr) old[j] = smem_hit(sm, u);
-    else if (ci && static_cast<uint32_t>(t[j]) >= V) ++invalid;
-  }
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const uint32_t u = static_cast<uint32_t>(t[j]) - lo;
-    if (u < Vr && ((old[j] >> ((u & 3u) << 3)) & 0xffu) == 0xffu)
-      settle_wrap(old[j], u >> 2, u & 3u, counts_pass, Vr);
-  }
-}
-
-__device__ __forceinline__ void count1(uint32_t* sm, int32_t t, uint32_t lo,
-                                       uint32_t Vr, uint32_t V, bool ci,
+// One token (loop tails).
+__device__ __forceinline__ void count1(uint32_t* sm, uint32_t t, uint32_t lo,
+                                       uint32_t Vr, uint32_t V,
                                        uint32_t* counts_pass,
-                                       uint32_t& invalid) {
-  const uint32_t u = static_cast<uint32_t>(t) - lo;
+                                       uint32_t& invalid, WrapCache& wc) {
+  const uint32_t u = t - lo;
   if (u < Vr) {
-    const uint32_t old = smem_hit(sm, u);
-    if (((old >> ((u & 3u) << 3)) & 0xffu) == 0xffu)
-      settle_wrap(old, u >> 2, u & 3u, counts_pass, Vr);
-  } else if (ci && static_cast<uint32_t>(t) >= V) {
+    const uint32_t sh = (u << 3) & 24u;
+    const uint32_t old = atomicAdd(&sm[u >> 2], 1u << sh);
+    if (((old >> sh) & 0xffu) == 0xffu)
+      settle_wrap(old, u >> 2, u & 3u, counts_pass, Vr, wc);
+  } else if (lo == 0 && t >= V) {
     ++invalid;
   }
 }
 
+template <bool kSingle>
 __global__ void __launch_bounds__(kCountThreads, 1)
     count_tokens_kernel(const int32_t* __restrict__ tokens, int64_t n,
                         uint32_t V, uint32_t lo, uint32_t Vr,
-                        int count_invalid, uint32_t* __restrict__ counts,
+                        uint32_t* __restrict__ counts,
                         unsigned long long* __restrict__ n_invalid,
                         uint32_t* __restrict__ slabs, int words_padded) {
   extern __shared__ __align__(16) uint32_t sm[];
+  __shared__ WrapCache wc;
   for (int i = threadIdx.x; i < words_padded; i += kCountThreads) sm[i] = 0;
+  for (int i = threadIdx.x; i < kCacheSlots; i += kCountThreads) {
+    wc.tag[i] = kEmptyTag;
+    wc.cnt[i] = 0u;
+  }
   __syncthreads();
 
   uint32_t* counts_pass = counts + lo;
   uint32_t invalid = 0;
-  const bool ci = count_invalid != 0;
   const int64_t n4 = n >> 2;
   const int4* t4 = reinterpret_cast<const int4*>(tokens);
   const int64_t stride = (int64_t)gridDim.x * kCountThreads;
   int64_t i = (int64_t)blockIdx.x * kCountThreads + threadIdx.x;
-  for (; i + 3 * stride < n4; i += 4 * stride) {
-    const int4 a = ld_stream_i4(t4 + i);
-    const int4 b = ld_stream_i4(t4 + i + stride);
-    const int4 c = ld_stream_i4(t4 + i + 2 * stride);
-    const int4 d = ld_stream_i4(t4 + i + 3 * stride);
-    const int32_t x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    count8(sm, x, lo, Vr, V, ci, counts_pass, invalid);
-    const int32_t y[8] = {c.x, c.y, c.z, c.w, d.x, d.y, d.z, d.w};
-    count8(sm, y, lo, Vr, V, ci, counts_pass, invalid);
+  // Steps of four int4 (16 tokens) per thread, two buffers in ping-pong:
+  // the loads of the next step are in flight while this step counts.
+  int4 a[4], b[4];
+  auto load4 = [&](int4 (&dst)[4], int64_t at) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) dst[q] = ld_stream_i4(t4 + at + q * stride);
+  };
+  const int64_t step = 4 * stride;
+  if (i + 3 * stride < n4) {
+    load4(a, i);
+    while (true) {
+      const bool more_b = i + step + 3 * stride < n4;
+      if (more_b) load4(b, i + step);
+      count16<kSingle>(sm, a, lo, Vr, V, counts_pass, invalid, wc);
+      i += step;
+      if (!more_b) break;
+      const bool more_a = i + step + 3 * stride < n4;
+      if (more_a) load4(a, i + step);
+      count16<kSingle>(sm, b, lo, Vr, V, counts_pass, invalid, wc);
+      i += step;
+      if (!more_a) break;
+    }
   }
   for (; i < n4; i += stride) {
-    const int4 a = ld_stream_i4(t4 + i);
-    count1(sm, a.x, lo, Vr, V, ci, counts_pass, invalid);
-    count1(sm, a.y, lo, Vr, V, ci, counts_pass, invalid);
-    count1(sm, a.z, lo, Vr, V, ci, counts_pass, invalid);
-    count1(sm, a.w, lo, Vr, V, ci, counts_pass, invalid);
+    const int4 x = ld_stream_i4(t4 + i);
+    count1(sm, (uint32_t)x.x, lo, Vr, V, counts_pass, invalid, wc);
+    count1(sm, (uint32_t)x.y, lo, Vr, V, counts_pass, invalid, wc);
+    count1(sm, (uint32_t)x.z, lo, Vr, V, counts_pass, invalid, wc);
+    count1(sm, (uint32_t)x.w, lo, Vr, V, counts_pass, invalid, wc);
   }
   if (blockIdx.x == 0 && threadIdx.x < (n & 3))
-    count1(sm, tokens[(n4 << 2) + threadIdx.x], lo, Vr, V, ci, counts_pass,
-           invalid);
+    count1(sm, (uint32_t)tokens[(n4 << 2) + threadIdx.x], lo, Vr, V,
+           counts_pass, invalid, wc);
   __syncthreads();
 
   uint32_t* slab = slabs + (size_t)blockIdx.x * words_padded;
   for (int w = threadIdx.x; w < words_padded; w += kCountThreads)
     slab[w] = sm[w];
+  for (int i = threadIdx.x; i < kCacheSlots; i += kCountThreads)
+    if (wc.tag[i] != kEmptyTag && wc.cnt[i] != 0u)
+      atomicAdd(&counts_pass[wc.tag[i]], wc.cnt[i]);
 
-  if (ci && n_invalid) {
+  if (lo == 0 && n_invalid) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) invalid += __shfl_xor_sync(~0u, invalid, o);
     if ((threadIdx.x & 31) == 0 && invalid)
@@ -217,9 +287,11 @@ extern "C" vt_status vt_count_tokens(const int32_t* tokens, int64_t n,
   if (n == 0) return VT_OK;
   DeviceInfo di;
   if (!current_device(&di)) return VT_ERR_CUDA;
-  const int ids_per_pass =
-      std::min<int>(kCountMaxIds, (di.max_smem_optin / 16) * 16);
-  if (!allow_max_smem(count_tokens_kernel, di)) return VT_ERR_CUDA;
+  const int ids_per_pass = std::min<int>(
+      kCountMaxIds, ((di.max_smem_optin - (int)sizeof(WrapCache)) / 16) * 16);
+  if (!allow_max_smem(count_tokens_kernel<true>, di) ||
+      !allow_max_smem(count_tokens_kernel<false>, di))
+    return VT_ERR_CUDA;
   const int G = (int)std::max<int64_t>(
       1, std::min<int64_t>({(int64_t)di.num_sms, (int64_t)kCountMaxCtas,
                             (n + kTokensPerCta - 1) / kTokensPerCta}));
@@ -228,8 +300,10 @@ extern "C" vt_status vt_count_tokens(const int32_t* tokens, int64_t n,
   for (int64_t lo = 0; lo < V; lo += ids_per_pass) {
     const uint32_t Vr = (uint32_t)std::min<int64_t>(ids_per_pass, V - lo);
     const int words = words_for(Vr);
-    count_tokens_kernel<<<G, kCountThreads, words * sizeof(uint32_t), s>>>(
-        tokens, n, (uint32_t)V, (uint32_t)lo, Vr, lo == 0, counts,
+    const bool single = lo == 0 && Vr == (uint32_t)V;
+    auto kern = single ? count_tokens_kernel<true> : count_tokens_kernel<false>;
+    kern<<<G, kCountThreads, words * sizeof(uint32_t), s>>>(
+        tokens, n, (uint32_t)V, (uint32_t)lo, Vr, counts,
         reinterpret_cast<unsigned long long*>(n_invalid), slabs, words);
     vt_status st = launch_status("count_tokens_kernel");
     if (st != VT_OK) return st;

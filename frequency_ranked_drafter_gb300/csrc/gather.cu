@@ -6,17 +6,17 @@
 //
 // HBM-bound copy: every kept row (d bf16 = 2d bytes) is read once and written
 // once.  One warp moves one row at a time with 16-byte loads; each lane keeps
-// up to 16 loads in flight before its stores, so a resident warp has 8 KB
-// outstanding.  The grid is a whole number of waves over the SMs.
+// 8 loads in flight before its stores (4 KB per warp), with 32 warps resident
+// per SM.  The grid is a whole number of waves over the SMs.
 #include "vt_common.cuh"
 
 namespace vt {
 namespace {
 
 constexpr int kGatherThreads = 256;
-constexpr int kGatherChunks = 16;  // 16-byte chunks per lane per step
+constexpr int kGatherChunks = 8;  // 16-byte chunks per lane per step
 
-__global__ void __launch_bounds__(kGatherThreads)
+__global__ void __launch_bounds__(kGatherThreads, 4)
     gather_rows_kernel(const uint16_t* __restrict__ W, int64_t V, int d,
                        const int32_t* __restrict__ t2f, int V_high,
                        uint16_t* __restrict__ W_high,
