@@ -317,8 +317,8 @@ def run_ours(args, world, rank, local):
     H = synth.normal_bf16((M, d), 1.0, seed=cfg.seed + 1, device=dev)
     ids = torch.empty(M, k, dtype=torch.int32, device=dev)
     probs = torch.empty(M, k, dtype=torch.float32, device=dev)
-    ws = torch.zeros(vt.workspace_bytes("head", M=M, k=k), dtype=torch.uint8,
-                     device=dev)
+    ws = torch.zeros(vt.workspace_bytes("head", M=M, k=k, V_high=V),
+                     dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
 
     def head_step(i):

@@ -69,7 +69,7 @@ def load(build_if_missing: bool = True):
             "vt_select_vocab_workspace_size": ([i32], sz),
             "vt_select_vocab": ([p, i32, i32, p, p, p, p, sz, p], ctypes.c_int),
             "vt_gather_rows": ([p, i64, i32, p, i32, p, p, p], ctypes.c_int),
-            "vt_draft_head_workspace_size": ([i32, i32], sz),
+            "vt_draft_head_workspace_size": ([i32, i32, i32], sz),
             "vt_draft_head": ([p, i32, i32, i64, p, i32, p, i32, p, p, p, p,
                                sz, p], ctypes.c_int),
         }
@@ -129,15 +129,17 @@ class Workspace:
 _ws = Workspace()
 
 
-def workspace_bytes(op: str, V: int = 0, M: int = 1, k: int = 1) -> int:
-    """Workspace size of op "count" (V), "select" (V) or "head" (M, k)."""
+def workspace_bytes(op: str, V: int = 0, M: int = 1, k: int = 1,
+                    V_high: int = 1) -> int:
+    """Workspace size of op "count" (V), "select" (V) or "head" (M, V_high,
+    k)."""
     lib = load()
     if op == "count":
         return lib.vt_count_tokens_workspace_size(V)
     if op == "select":
         return lib.vt_select_vocab_workspace_size(V)
     if op == "head":
-        return lib.vt_draft_head_workspace_size(M, k)
+        return lib.vt_draft_head_workspace_size(M, V_high, k)
     raise ValueError(op)
 
 
@@ -236,7 +238,7 @@ def draft_head(H: torch.Tensor, W_high: torch.Tensor, t2f: torch.Tensor | None,
     if out_logits is not None:
         _cuda(out_logits, "out_logits", torch.float32)
     lib = load()
-    nbytes = lib.vt_draft_head_workspace_size(M, k)
+    nbytes = lib.vt_draft_head_workspace_size(M, V_high, k)
     if ws is None:
         ws = _ws.get("head", nbytes, dev, zeroed=True)
     _check("vt_draft_head", lib.vt_draft_head(

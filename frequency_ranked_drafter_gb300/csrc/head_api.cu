@@ -1,8 +1,10 @@
 // vt_draft_head entry point: argument checks, workspace layout, dispatch.
 #include "head_common.cuh"
 
-extern "C" size_t vt_draft_head_workspace_size(int32_t M, int32_t k) {
-  if (M <= 0 || k <= 0) return 0;
+extern "C" size_t vt_draft_head_workspace_size(int32_t M, int32_t V_high,
+                                               int32_t k) {
+  if (M <= 0 || V_high <= 0 || k <= 0) return 0;
+  if (M >= vt::kHeadTcMinM) return vt::head_tc_workspace(M, V_high);
   return (size_t)vt::kHeadTicketBytes +
          (size_t)vt::kHeadMaxCtas * M * vt::head_pstride(k) * sizeof(float);
 }
@@ -30,12 +32,16 @@ extern "C" vt_status vt_draft_head(const uint16_t* H, int32_t M, int32_t d,
                 "vt_draft_head: need 1 <= k <= 32 and k <= V_high");
   if (!aligned(H, 16) || !aligned(W_high, 16))
     return fail(VT_ERR_INVALID_ARG, "vt_draft_head: H, W_high not 16B aligned");
-  if (!ws || !aligned(ws, 256) || ws_bytes < vt_draft_head_workspace_size(M, k))
+  if (!ws || !aligned(ws, 256) ||
+      ws_bytes < vt_draft_head_workspace_size(M, V_high, k))
     return fail(VT_ERR_WORKSPACE,
                 "vt_draft_head: workspace missing, misaligned or too small");
   DeviceInfo di;
   if (!current_device(&di)) return VT_ERR_CUDA;
   cudaStream_t s = (cudaStream_t)stream;
+  if (M >= kHeadTcMinM)
+    return head_tc(H, M, d, ldh, W_high, V_high, t2f, k, out_ids, out_probs,
+                   out_logits, ws, di, s);
 
   HeadArgs a;
   a.ldh = ldh;
@@ -47,7 +53,7 @@ extern "C" vt_status vt_draft_head(const uint16_t* H, int32_t M, int32_t d,
   a.pstride = head_pstride(k);
   a.ticket = static_cast<unsigned*>(ws);
   a.part = reinterpret_cast<float*>(static_cast<char*>(ws) + kHeadTicketBytes);
-  // Hidden states go through the GEMV path four at a time.
+  // A few hidden states: the GEMV path.
   for (int m0 = 0; m0 < M; m0 += 4) {
     a.M = std::min(4, M - m0);
     a.H = H + (int64_t)m0 * ldh;

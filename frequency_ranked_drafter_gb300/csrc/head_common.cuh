@@ -257,4 +257,14 @@ __device__ void head_final_merge(const HeadArgs& a, int MR, int G,
 // Small-M GEMV path (M <= 4), head_gemv.cu.
 vt_status head_gemv(const HeadArgs& a, const DeviceInfo& di, cudaStream_t s);
 
+// Tree-draft tensor-core path (M >= kHeadTcMinM), head_tc.cu.  The
+// workspace holds an error word at byte 128 and, when out_logits is null,
+// the [M, V_high] fp32 logits from byte 256 on.
+constexpr int kHeadTcMinM = 5;
+size_t head_tc_workspace(int M, int V_high);
+vt_status head_tc(const uint16_t* H, int M, int d, int64_t ldh,
+                  const uint16_t* W, int V_high, const int32_t* t2f, int k,
+                  int32_t* out_ids, float* out_probs, float* out_logits,
+                  void* ws, const DeviceInfo& di, cudaStream_t s);
+
 }  // namespace vt

@@ -92,9 +92,9 @@ extern "C" vt_status vt_draft_head_noalloc(const uint16_t* H, int32_t M,
   if (!aligned(H, 16) || !aligned(W_high, 16))
     return fail(VT_ERR_INVALID_ARG,
                 "vt_draft_head_noalloc: H, W_high not 16B aligned");
-  // Hidden states are processed four at a time, each group reusing the
-  // same scratch, so the need depends on min(M, 4) and k only.
-  const size_t need = vt_draft_head_workspace_size(std::min(M, 4), k);
+  // Hidden states are processed four at a time by the GEMV kernel, each
+  // group reusing the same scratch, so the need depends on min(M, 4) and k.
+  const size_t need = vt_draft_head_workspace_size(std::min(M, 4), V_high, k);
   if (need > kNoAllocScratchBytes)
     return fail(VT_ERR_UNSUPPORTED,
                 "vt_draft_head_noalloc: needs " + std::to_string(need) +

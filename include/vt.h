@@ -151,11 +151,19 @@ vt_status vt_gather_rows(const uint16_t* W, int64_t V, int32_t d,
  *   out_probs (device) float[M, k].
  *   out_logits(device, nullable) float[M, V_high]: every trimmed logit, for
  *             verification; costs an extra write of M*V_high*4 bytes.
- *   ws        (device) workspace of vt_draft_head_workspace_size(M, k)
- *             bytes.  It must be zero-filled once before its first use;
- *             every call leaves it zero-filled again.
+ *   ws        (device) workspace of vt_draft_head_workspace_size(M, V_high,
+ *             k) bytes.  It must be zero-filled once before its first use;
+ *             the counters it holds are left zero by every call.  For
+ *             M >= 5 it also holds the [M, V_high] fp32 logits (when
+ *             out_logits is NULL), and the 32-bit word at byte 128 is a
+ *             device error word: 0, or VT_ERR_TIMEOUT if a bounded wait
+ *             inside the kernel gave up (readable after a synchronise).
+ *
+ * Paths: M <= 4 runs a split-V GEMV (CUDA cores, one launch); M >= 5 runs a
+ * tcgen05 tensor-core GEMM over all M rows at once plus a per-row softmax
+ * and top-k kernel.
  * ------------------------------------------------------------------------ */
-size_t vt_draft_head_workspace_size(int32_t M, int32_t k);
+size_t vt_draft_head_workspace_size(int32_t M, int32_t V_high, int32_t k);
 vt_status vt_draft_head(const uint16_t* H, int32_t M, int32_t d, int64_t ldh,
                         const uint16_t* W_high, int32_t V_high,
                         const int32_t* t2f, int32_t k, int32_t* out_ids,
@@ -174,9 +182,10 @@ vt_status vt_draft_head(const uint16_t* H, int32_t M, int32_t d, int64_t ldh,
  * computes, with the same arguments minus the workspace, and allocates
  * nothing: its scratch is one fixed 1 MiB array in device memory that the
  * library defines and every GPU that loads the library keeps until exit.
+ * It always runs the GEMV kernel, four hidden states at a time.
  *
- *   Limit     the scratch needed, vt_draft_head_workspace_size(min(M, 4), k),
- *             must fit in 1 MiB (any k <= 32 for M <= 3; k <= 30 for
+ *   Limit     the scratch needed, vt_draft_head_workspace_size(min(M, 4),
+ *             V_high, k), must fit in 1 MiB (any k <= 32 for M <= 3; k <= 30 for
  *             M >= 4); larger requests return VT_ERR_UNSUPPORTED.
  *   Set-up    the first call on each device looks up the array's device
  *             address and zero-fills its counters with a synchronous

@@ -28,14 +28,24 @@ def logit_tol(ref):
     return LOGIT_RTOL * (1.0 + np.abs(ref))
 
 
-def check_logits(gpu_logits: np.ndarray, ref: np.ndarray):
-    bad = np.abs(gpu_logits.astype(np.float64) - ref) > logit_tol(ref)
+def fp32_sum_bound(H_bits: np.ndarray, W_bits: np.ndarray) -> np.ndarray:
+    """Worst-case error of summing d products in fp32 (any order):
+    d * 2^-24 * sum_j |h_j * w_j| for every logit.  Far below the logit
+    tolerance for the workloads' N(0, 1) x N(0, 0.02) inputs; it only
+    matters for inputs built to give huge, cancelling terms."""
+    h = (H_bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    w = (W_bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return h.shape[1] * 2.0 ** -24 * (np.abs(h) @ np.abs(w).T)
+
+
+def check_logits(gpu_logits: np.ndarray, ref: np.ndarray, extra=0.0):
+    bad = np.abs(gpu_logits.astype(np.float64) - ref) > logit_tol(ref) + extra
     assert not bad.any(), (
         f"{bad.sum()} logits out of tolerance; worst at "
         f"{np.unravel_index(np.argmax(np.abs(gpu_logits - ref)), ref.shape)}")
 
 
-def check_topk(ids, probs, ref_logits, t2f, oracle_res, k):
+def check_topk(ids, probs, ref_logits, t2f, oracle_res, k, extra=None):
     """GPU top-k of each row against the oracle.
 
     ``ref_logits`` [M, V_high] are the oracle's fp64 trimmed logits.  Rank r
@@ -63,7 +73,8 @@ def check_topk(ids, probs, ref_logits, t2f, oracle_res, k):
             row = gid if full_to_row is None else full_to_row.get(gid)
             assert row is not None and 0 <= row < V_high, f"row {m}: id {gid} not kept"
             lv = ref_logits[m, row]
-            assert abs(lv - o_log[r]) <= logit_tol(o_log[r]), (
+            widen = 0.0 if extra is None else extra[m, row] + extra[m].max()
+            assert abs(lv - o_log[r]) <= logit_tol(o_log[r]) + widen, (
                 f"row {m} rank {r}: gpu id {gid} (logit {lv}) vs oracle id "
                 f"{o_ids[r]} (logit {o_log[r]})")
             p_ref = np.exp(lv - mx) / se

@@ -51,13 +51,14 @@ def test_workspace_sizes(lib):
     assert lib.vt_count_tokens_workspace_size(0) == 0
     assert lib.vt_count_tokens_workspace_size(128256) >= 128256
     assert lib.vt_select_vocab_workspace_size(128256) >= 16 * 128256
-    assert lib.vt_draft_head_workspace_size(1, 10) > 256
-    assert (lib.vt_draft_head_workspace_size(64, 10)
-            > lib.vt_draft_head_workspace_size(1, 10))
+    assert lib.vt_draft_head_workspace_size(1, 32768, 10) > 256
+    # the tensor-core path (M >= 5) keeps the [M, V_high] fp32 logits
+    assert lib.vt_draft_head_workspace_size(64, 32768, 10) >= 64 * 32768 * 4
+    assert lib.vt_draft_head_workspace_size(0, 32768, 10) == 0
 
 
 def test_draft_head_rejects_bad_arguments(lib):
-    ws_ok = lib.vt_draft_head_workspace_size(1, 10)
+    ws_ok = lib.vt_draft_head_workspace_size(1, 32768, 10)
 
     def call(H=FAKE, M=1, d=4096, ldh=4096, W=FAKE, V_high=32768, t2f=None,
              k=10, ids=FAKE, probs=FAKE, logits=None, ws=FAKE, ws_bytes=ws_ok):

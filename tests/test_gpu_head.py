@@ -10,13 +10,14 @@ import torch
 import frequency_ranked_drafter_gb300 as vt
 import oracle
 import synth
-from gpu_util import bits_host, check_logits, check_topk, need_cuda
+from gpu_util import (bits_host, check_logits, check_topk, fp32_sum_bound,
+                      need_cuda)
 
 pytestmark = pytest.mark.gpu
 
 
 def run_case(d, V_high, M, k, seed, hs=1.0, ws=0.02, use_t2f=True,
-             V=None, ldh=None, want_logits=True, check_rows=None):
+             V=None, ldh=None, want_logits=True, check_rows=None, widen=False):
     dev = need_cuda()
     V = V or max(V_high, 2 * V_high)
     W_high = synth.normal_bf16((V_high, d), ws, seed=seed, device=dev)
@@ -35,10 +36,12 @@ def run_case(d, V_high, M, k, seed, hs=1.0, ws=0.02, use_t2f=True,
     t2f_h = None if t2f is None else t2f.cpu().numpy()
     ref = oracle.draft_head(Hh, Wh, t2f_h, k)
     ref_logits = oracle.head_logits(Hh, Wh)
+    extra = fp32_sum_bound(Hh, Wh) if widen else None
     if want_logits:
-        check_logits(logits.cpu().numpy()[rows], ref_logits)
+        check_logits(logits.cpu().numpy()[rows], ref_logits,
+                     0.0 if extra is None else extra)
     exact = check_topk(ids.cpu().numpy()[rows], probs.cpu().numpy()[rows],
-                       ref_logits, t2f_h, ref, k)
+                       ref_logits, t2f_h, ref, k, extra)
     return exact, ids, probs
 
 
@@ -89,7 +92,8 @@ def test_head_many_hidden_states_grouped():
 
 
 def test_head_large_logits_no_overflow():
-    exact, _, probs = run_case(1024, 4000, 1, 10, seed=11, hs=64.0, ws=1.0)
+    exact, _, probs = run_case(1024, 4000, 1, 10, seed=11, hs=64.0, ws=1.0,
+                               widen=True)
     assert torch.isfinite(probs).all()
 
 

@@ -1,0 +1,101 @@
+"""GPU parity of the tree-draft (tensor-core) head path, M >= 5 hidden
+states, against the CPU oracle through the C ABI: logits within
+1e-3 * (1 + |l|), probabilities within 1e-4, top-k ids equal to the
+oracle's except where oracle logits are closer than that tolerance.  Sizes
+cover ragged K blocks (d not a multiple of 64), ragged last tiles (V_high
+not a multiple of 128), N = M rounded up to 16 from 16 to 256, and the
+full EAGLE-2 tree-draft shapes (sampled hidden states)."""
+import numpy as np
+import pytest
+import torch
+
+import frequency_ranked_drafter_gb300 as vt
+import oracle
+import synth
+from gpu_util import (bits_host, check_logits, check_topk, fp32_sum_bound,
+                      need_cuda)
+
+pytestmark = pytest.mark.gpu
+
+
+def run_tc(d, V_high, M, k, seed, rows=None, use_t2f=True, want_logits=True,
+           hs=1.0, ws_scale=0.02, widen=False):
+    dev = need_cuda()
+    W_high = synth.normal_bf16((V_high, d), ws_scale, seed=seed, device=dev)
+    H = synth.normal_bf16((M, d), hs, seed=seed + 1, device=dev)
+    t2f = (synth.rank_permutation(2 * V_high, seed)[:V_high].to(dev)
+           if use_t2f else None)
+    ws = torch.zeros(vt.workspace_bytes("head", M=M, k=k, V_high=V_high),
+                     dtype=torch.uint8, device=dev)
+    logits = (torch.empty(M, V_high, dtype=torch.float32, device=dev)
+              if want_logits else None)
+    ids, probs = vt.draft_head(H, W_high, t2f, k, out_logits=logits, ws=ws)
+    torch.cuda.synchronize()
+    err = int(ws[128:132].view(torch.int32).item())
+    assert err == 0, f"device error word {err}"
+    rows = list(range(M)) if rows is None else rows
+    Hh, Wh = bits_host(H[rows]), bits_host(W_high)
+    t2f_h = None if t2f is None else t2f.cpu().numpy()
+    ref = oracle.draft_head(Hh, Wh, t2f_h, k)
+    ref_logits = oracle.head_logits(Hh, Wh)
+    extra = fp32_sum_bound(Hh, Wh) if widen else None
+    if want_logits:
+        check_logits(logits.cpu().numpy()[rows], ref_logits,
+                     0.0 if extra is None else extra)
+    check_topk(ids.cpu().numpy()[rows], probs.cpu().numpy()[rows], ref_logits,
+               t2f_h, ref, k, extra)
+    return ids, probs
+
+
+@pytest.mark.parametrize("d,V_high,M,k", [
+    (256, 1024, 5, 8),       # smallest M on this path: N = 16
+    (1032, 3001, 16, 10),    # ragged K block and ragged last tile
+    (2048, 4096, 33, 10),    # N = 48
+    (520, 777, 64, 1),       # greedy, one partial tile only
+    (3584, 2000, 128, 32),   # N = 128, k = 32
+    (512, 1500, 256, 5),     # N = 256, the widest MMA
+])
+def test_tc_shapes(d, V_high, M, k):
+    run_tc(d, V_high, M, k, seed=d + V_high + M)
+
+
+def test_tc_identity_map():
+    run_tc(1024, 5000, 24, 10, seed=3, use_t2f=False)
+
+
+def test_tc_large_logits_no_overflow():
+    """Huge, cancelling products: logits are held to the fp32 summation
+    bound on top of the usual tolerance; the softmax must not overflow."""
+    _, probs = run_tc(1024, 3000, 8, 10, seed=4, hs=64.0, ws_scale=1.0,
+                      widen=True)
+    assert torch.isfinite(probs).all()
+
+
+def test_tc_repeated_calls_identical():
+    dev = need_cuda()
+    W = synth.normal_bf16((10000, 2048), 0.02, seed=7, device=dev)
+    H = synth.normal_bf16((20, 2048), 1.0, seed=8, device=dev)
+    a = [t.clone() for t in vt.draft_head(H, W, None, 10)]
+    for _ in range(3):
+        ids, probs = vt.draft_head(H, W, None, 10)
+        assert torch.equal(ids, a[0]) and torch.equal(probs, a[1])
+
+
+def test_tc_eagle2_tree_m60_v_high_sweep():
+    """EAGLE-2-style tree draft, d = 4096, M = 60, over the V_high sweep
+    (8192 .. 65536); four sampled hidden states against the oracle."""
+    for V_high in (8192, 16384, 32768, 65536):
+        run_tc(4096, V_high, 60, 10, seed=1003 + V_high, rows=[0, 21, 42, 59],
+               want_logits=False)
+
+
+def test_tc_full_vocab_m60_sampled():
+    run_tc(4096, 128256, 60, 10, seed=1003, rows=[7, 58], want_logits=False,
+           use_t2f=False)
+
+
+@pytest.mark.parametrize("shape", [synth.QWEN7B_HEAD, synth.LLAMA1B_HEAD])
+@pytest.mark.parametrize("M", [16, 64])
+def test_tc_qwen_and_llama1b_batch_sweep(shape, M):
+    run_tc(shape.d, shape.V_high, M, shape.k, seed=shape.seed + M,
+           rows=[0, M // 2, M - 1], want_logits=False)
