@@ -4,7 +4,7 @@
 extern "C" size_t vt_draft_head_workspace_size(int32_t M, int32_t V_high,
                                                int32_t k) {
   if (M <= 0 || V_high <= 0 || k <= 0) return 0;
-  if (M >= vt::kHeadTcMinM) return vt::head_tc_workspace(M, V_high);
+  if (M >= vt::kHeadTcMinM) return vt::head_tc_workspace(M, V_high, k);
   return (size_t)vt::kHeadTicketBytes +
          (size_t)vt::kHeadMaxCtas * M * vt::head_pstride(k) * sizeof(float);
 }

@@ -12,7 +12,12 @@ namespace vt {
 
 constexpr int kTopKMax = 32;
 constexpr int kHeadMaxCtas = 1024;
-constexpr int kHeadTicketBytes = 256;
+// Workspace header shared by both head paths, so one workspace can serve
+// calls of any M: bytes [0, 8) GEMV counters, [128, 132) tensor-core path
+// error word, [1024, 2048) tensor-core per-row counters (M <= 256).  Every
+// counter is zero between calls; nothing else is written in the header.
+constexpr int kHeadTicketBytes = 2048;
+constexpr int kHeadRowTicketOffset = 1024;
 constexpr int kStageBytesMax = 96 * 1024;  // staged candidates, last CTA
 
 // Each CTA publishes, per hidden state m, `pstride` 32-bit words:
@@ -254,14 +259,14 @@ __device__ void head_final_merge(const HeadArgs& a, int MR, int G,
   }
 }
 
-// Small-M GEMV path (M <= 4), head_gemv.cu.
+// CUDA-core GEMV path (M = 1 in vt_draft_head; up to 4 per launch), head_gemv.cu.
 vt_status head_gemv(const HeadArgs& a, const DeviceInfo& di, cudaStream_t s);
 
 // Tree-draft tensor-core path (M >= kHeadTcMinM), head_tc.cu.  The
-// workspace holds an error word at byte 128 and, when out_logits is null,
-// the [M, V_high] fp32 logits from byte 256 on.
-constexpr int kHeadTcMinM = 5;
-size_t head_tc_workspace(int M, int V_high);
+// workspace holds an error word at byte 128, per-row counters and partials
+// and, when out_logits is null, the [M, V_high] fp32 logits.
+constexpr int kHeadTcMinM = 2;
+size_t head_tc_workspace(int M, int V_high, int k);
 vt_status head_tc(const uint16_t* H, int M, int d, int64_t ldh,
                   const uint16_t* W, int V_high, const int32_t* t2f, int k,
                   int32_t* out_ids, float* out_probs, float* out_logits,

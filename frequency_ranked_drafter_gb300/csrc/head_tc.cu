@@ -1,4 +1,4 @@
-// vt_draft_head, tree-draft path (M >= 5 hidden states): a tcgen05 GEMM for
+// vt_draft_head, tree-draft path (M >= 2 hidden states): a tcgen05 GEMM for
 // the logits of all M rows at once, then a per-row softmax + top-k kernel.
 //
 // "FR-Spec: Accelerating Large-Vocabulary Language Models via
@@ -19,12 +19,9 @@
 // fp32 logits (tile rows along lanes, so every store is a coalesced 128-byte
 // row segment).  At these M the work stays bound by the W_high stream.
 //
-// Softmax + top-k: one CTA per hidden state reads its V_high logits twice
-// from L2: the first pass builds the online (max, sum of exp) and each
-// thread's best entry; a warp tournament over those bests gives a lower
-// bound on the k-th best logit (a warp's k-th best thread-best has k
-// entries at least as good); the second pass keeps only entries reaching
-// that bound, which are ranked exactly by counting.
+// Softmax + top-k: each hidden state's V_high logits (L2-resident) are
+// split over CTAs of 4096; each CTA reduces its part to (max, sum of exp,
+// exact top-k) and the last CTA of the row merges the parts.
 //
 // Every wait on an mbarrier is bounded (kWaitBudget cycles, about a
 // second); a wait that gives up records VT_ERR_TIMEOUT in the error word of
@@ -215,40 +212,82 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 }
 
 // ------------------------------------------------- per-row softmax + top-k
-constexpr int kRowThreads = 512;
-constexpr int kRowSurvivors = 4096;
+// Grid: M rows x P parts.  Each CTA owns kRowSpan consecutive logits of one
+// row (kRowVals per thread, loaded once into registers with float4 loads),
+// computes their (max, sum of exp) and their exact top-k, publishes them as
+// a partial, and the last CTA of the row to arrive (ticket per row, acquire
+// -release) merges the row's P partials and writes ids and probabilities.
+//
+// Exact top-k of a CTA's values: each warp's k-th best thread-best (a warp
+// tournament with redux.sync) bounds the CTA's k-th best from below (those k
+// thread-bests are k values at least that good); only values reaching the
+// best such bound are kept, and they are ranked by counting.
+constexpr int kRowThreads = 256;
+constexpr int kRowVals = 16;
+constexpr int kRowSpan = kRowThreads * kRowVals;  // 4096 logits per CTA
+constexpr int kRowSurvivors = 2048;
+
+struct RowArgs {
+  const float* logits;  // [M][V_high]
+  int V_high, k, P;
+  const int32_t* t2f;
+  int32_t* out_ids;
+  float* out_probs;
+  unsigned* tickets;  // [M], zero between calls
+  float* part;        // [M][P][2 + 2k]
+};
 
 __global__ void __launch_bounds__(kRowThreads)
-    rows_topk_kernel(const float* __restrict__ logits, int V_high, int k,
-                     const int32_t* __restrict__ t2f,
-                     int32_t* __restrict__ out_ids,
-                     float* __restrict__ out_probs) {
+    rows_topk_kernel(RowArgs a) {
   constexpr int kWarps = kRowThreads / 32;
   __shared__ float red[kWarps];
   __shared__ float tw_v[kWarps];
   __shared__ int tw_i[kWarps];
   __shared__ float2 surv[kRowSurvivors];
-  __shared__ int s_cnt;
+  __shared__ int s_cnt, s_last;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const float* row = logits + (size_t)blockIdx.x * V_high;
-  int32_t* ids = out_ids + (size_t)blockIdx.x * k;
-  float* probs = out_probs + (size_t)blockIdx.x * k;
+  const int m = blockIdx.y, part_idx = blockIdx.x, k = a.k;
+  const int ps = 2 + 2 * k;
+  const float* row = a.logits + (size_t)m * a.V_high;
+  const int base = part_idx * kRowSpan;
 
-  // pass 1: online (max, sumexp) and this thread's best entry
-  float mx = -INFINITY, se = 0.f, bv = -INFINITY;
+  // this thread's values: 4 float4 at base + 4*(tid + 256*q) (or scalars
+  // when the row is not 16-byte aligned or at the tail)
+  float v[kRowVals];
+  const bool vec = ((a.V_high & 3) == 0) &&
+                   ((reinterpret_cast<uintptr_t>(a.logits) & 15) == 0);
+#pragma unroll
+  for (int q = 0; q < kRowVals / 4; ++q) {
+    const int i0 = base + 4 * (tid + kRowThreads * q);
+    if (vec && i0 + 3 < a.V_high) {
+      const float4 x = __ldcg(reinterpret_cast<const float4*>(row + i0));
+      v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        v[4 * q + e] = i0 + e < a.V_high ? __ldcg(row + i0 + e) : -INFINITY;
+    }
+  }
+  auto idx_of = [&](int j) { return base + 4 * (tid + kRowThreads * (j >> 2)) + (j & 3); };
+
+  float mx = -INFINITY, bv = -INFINITY;
   int bi = INT_MAX;
-  for (int i = tid; i < V_high; i += kRowThreads) {
-    const float v = __ldcg(row + i);
-    if (v > mx) { se = se * __expf(mx - v) + 1.f; mx = v; }
-    else se += __expf(v - mx);
-    if (v > bv) { bv = v; bi = i; }  // i grows: the first of equals stays
+#pragma unroll
+  for (int j = 0; j < kRowVals; ++j) {
+    mx = fmaxf(mx, v[j]);
+    const int i = idx_of(j);
+    if (i < a.V_high && key_beats(v[j], i, bv, bi)) { bv = v[j]; bi = i; }
+  }
+  float se = 0.f;
+  if (mx > -INFINITY) {
+#pragma unroll
+    for (int j = 0; j < kRowVals; ++j) se += __expf(v[j] - mx);
   }
   if (tid == 0) s_cnt = 0;
-  const float mg = block_max<kRowThreads>(mx, red);
-  const float sg = block_sum<kRowThreads>(se > 0.f ? se * __expf(mx - mg) : 0.f, red);
+  const float cm = block_max<kRowThreads>(mx, red);
+  const float cs = block_sum<kRowThreads>(se > 0.f ? se * __expf(mx - cm) : 0.f, red);
 
-  // lower bound on the k-th best: per warp, the k-th best thread-best
-  {
+  {  // per-warp bound: the k-th best thread-best of the warp
     float tv = -INFINITY;
     int ti = INT_MAX;
     float lv = bv;
@@ -256,65 +295,89 @@ __global__ void __launch_bounds__(kRowThreads)
     for (int r = 0; r < k; ++r) {
       const unsigned lk = li != INT_MAX ? float_key(lv) : 0u;
       const unsigned wk = __reduce_max_sync(~0u, lk);
-      if (wk == 0u) { tv = -INFINITY; ti = INT_MAX; break; }  // fewer than k
+      if (wk == 0u) { tv = -INFINITY; ti = INT_MAX; break; }
       const int wi = (int)__reduce_min_sync(~0u, lk == wk ? (unsigned)li : 0xffffffffu);
       const unsigned owner = __ballot_sync(~0u, lk == wk && li == wi);
-      const float wv = __shfl_sync(~0u, lv, __ffs(owner) - 1);
-      tv = wv;
+      tv = __shfl_sync(~0u, lv, __ffs(owner) - 1);
       ti = wi;
       if (lk == wk && li == wi) { lv = -INFINITY; li = INT_MAX; }
     }
     if (lane == 0) { tw_v[warp] = tv; tw_i[warp] = ti; }
   }
   __syncthreads();
-  float T_v = tw_v[0];
-  int T_i = tw_i[0];
-  for (int w = 1; w < kWarps; ++w)
+  float T_v = -INFINITY;
+  int T_i = INT_MAX;
+  for (int w = 0; w < kWarps; ++w)
     if (tw_i[w] != INT_MAX && key_beats(tw_v[w], tw_i[w], T_v, T_i)) {
       T_v = tw_v[w]; T_i = tw_i[w];
     }
-
-  // pass 2: entries not beaten by the bound
-  for (int i = tid; i < V_high; i += kRowThreads) {
-    const float v = __ldcg(row + i);
-    if (!key_beats(T_v, T_i, v, i)) {
+#pragma unroll
+  for (int j = 0; j < kRowVals; ++j) {
+    const int i = idx_of(j);
+    if (i < a.V_high && !key_beats(T_v, T_i, v[j], i)) {
       const int p = atomicAdd(&s_cnt, 1);
-      if (p < kRowSurvivors) surv[p] = make_float2(v, __int_as_float(i));
+      if (p < kRowSurvivors) surv[p] = make_float2(v[j], __int_as_float(i));
     }
   }
   __syncthreads();
-  const int S = s_cnt;
-  if (S <= kRowSurvivors) {
-    for (int c = tid; c < S; c += kRowThreads) {
-      const float v = surv[c].x;
-      const int i = __float_as_int(surv[c].y);
-      int rank = 0;
-      for (int q = 0; q < S; ++q)
-        rank += key_beats(surv[q].x, __float_as_int(surv[q].y), v, i);
-      if (rank < k) {
-        ids[rank] = t2f ? t2f[i] : i;
-        probs[rank] = expf(v - mg) / sg;
-      }
-    }
-  } else {  // more survivors than the buffer (pathological): k arg-max rounds
-    float pv = INFINITY;
-    int pi = INT_MIN;
-    for (int r = 0; r < k; ++r) {
-      float bv2 = -INFINITY;
-      int bi2 = INT_MAX;
-      for (int i = tid; i < V_high; i += kRowThreads) {
-        const float v = __ldcg(row + i);
-        if (key_beats(pv, pi, v, i) && key_beats(v, i, bv2, bi2)) { bv2 = v; bi2 = i; }
-      }
-      block_best<kRowThreads>(bv2, bi2, tw_v, tw_i);
-      if (tid == 0) {
-        ids[r] = bi2 == INT_MAX ? -1 : (t2f ? t2f[bi2] : bi2);
-        probs[r] = bi2 == INT_MAX ? 0.f : expf(bv2 - mg) / sg;
-      }
-      pv = bv2;
-      pi = bi2;
+  float* mypart = a.part + ((size_t)m * a.P + part_idx) * ps;
+  const int S = min(s_cnt, kRowSurvivors);
+  // slots this CTA cannot fill stay (-inf, INT_MAX)
+  for (int r = tid; r < k; r += kRowThreads) {
+    mypart[2 + r] = -INFINITY;
+    reinterpret_cast<int*>(mypart)[2 + k + r] = INT_MAX;
+  }
+  __syncthreads();
+  for (int c = tid; c < S; c += kRowThreads) {
+    const float x = surv[c].x;
+    const int i = __float_as_int(surv[c].y);
+    int rank = 0;
+    for (int q = 0; q < S; ++q) rank += key_beats(surv[q].x, __float_as_int(surv[q].y), x, i);
+    if (rank < k) {
+      mypart[2 + rank] = x;
+      reinterpret_cast<int*>(mypart)[2 + k + rank] = i;
     }
   }
+  if (tid == 0) { mypart[0] = cm; mypart[1] = cs; }
+
+  // ---- last CTA of the row merges the row's P partials
+  __syncthreads();
+  if (tid == 0) s_last = ticket_arrive(a.tickets + m) == (unsigned)(a.P - 1);
+  __syncthreads();
+  if (!s_last) return;
+  const float* rp = a.part + (size_t)m * a.P * ps;
+  float pm = -INFINITY, psum = 0.f;
+  for (int b = tid; b < a.P; b += kRowThreads) pm = fmaxf(pm, __ldcg(rp + (size_t)b * ps));
+  const float mg = block_max<kRowThreads>(pm, red);
+  for (int b = tid; b < a.P; b += kRowThreads) {
+    const float s = __ldcg(rp + (size_t)b * ps + 1);
+    if (s > 0.f) psum += s * __expf(__ldcg(rp + (size_t)b * ps) - mg);
+  }
+  const float sg = block_sum<kRowThreads>(psum, red);
+  if (tid == 0) s_cnt = 0;
+  __syncthreads();
+  const int nc = a.P * k;  // all partial candidates (P*k <= kRowSurvivors)
+  for (int c = tid; c < nc; c += kRowThreads) {
+    const int b = c / k, r = c - b * k;
+    const float x = __ldcg(rp + (size_t)b * ps + 2 + r);
+    const int i = __ldcg(reinterpret_cast<const int*>(rp + (size_t)b * ps) + 2 + k + r);
+    surv[c] = make_float2(x, __int_as_float(i));
+  }
+  __syncthreads();
+  int32_t* ids = a.out_ids + (size_t)m * k;
+  float* probs = a.out_probs + (size_t)m * k;
+  for (int c = tid; c < nc; c += kRowThreads) {
+    const float x = surv[c].x;
+    const int i = __float_as_int(surv[c].y);
+    if (i == INT_MAX) continue;
+    int rank = 0;
+    for (int q = 0; q < nc; ++q) rank += key_beats(surv[q].x, __float_as_int(surv[q].y), x, i);
+    if (rank < k) {
+      ids[rank] = a.t2f ? a.t2f[i] : i;
+      probs[rank] = expf(x - mg) / sg;
+    }
+  }
+  if (tid == 0) a.tickets[m] = 0u;
 }
 
 // ------------------------------------------------------- host side
@@ -350,8 +413,25 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
 
 }  // namespace
 
-size_t head_tc_workspace(int M, int V_high) {
-  return 256 + (size_t)M * V_high * sizeof(float);
+// Workspace of the tensor-core path: the shared header (error word at byte
+// 128, per-row tickets from byte 1024), then per-row partials of the top-k
+// kernel, then the fp32 logits.
+struct TcLayout {
+  size_t tickets, part, logits, total;
+};
+static size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+static int row_parts(int V_high) { return (V_high + kRowSpan - 1) / kRowSpan; }
+static TcLayout tc_layout(int M, int V_high, int k) {
+  TcLayout L;
+  L.tickets = kHeadRowTicketOffset;
+  L.part = kHeadTicketBytes;
+  L.logits = L.part + round256((size_t)M * row_parts(V_high) * (2 + 2 * k) * 4);
+  L.total = L.logits + (size_t)M * V_high * 4;
+  return L;
+}
+
+size_t head_tc_workspace(int M, int V_high, int k) {
+  return tc_layout(M, V_high, k).total;
 }
 
 vt_status head_tc(const uint16_t* H, int M, int d, int64_t ldh,
@@ -359,9 +439,13 @@ vt_status head_tc(const uint16_t* H, int M, int d, int64_t ldh,
                   int32_t* out_ids, float* out_probs, float* out_logits,
                   void* ws, const DeviceInfo& di, cudaStream_t s) {
   if (M > 256) return fail(VT_ERR_UNSUPPORTED, "head_tc: M > 256");
-  unsigned* err = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + 128);
-  float* logits = out_logits ? out_logits
-                             : reinterpret_cast<float*>(static_cast<char*>(ws) + 256);
+  const TcLayout L = tc_layout(M, V_high, k);
+  char* wsb = static_cast<char*>(ws);
+  unsigned* err = reinterpret_cast<unsigned*>(wsb + 128);
+  float* logits = out_logits ? out_logits : reinterpret_cast<float*>(wsb + L.logits);
+  const int P = row_parts(V_high);
+  if (P * k > kRowSurvivors)
+    return fail(VT_ERR_UNSUPPORTED, "head_tc: V_high * k too large for the row merge");
   TcArgs a;
   a.V_high = V_high;
   a.d = d;
@@ -387,8 +471,17 @@ vt_status head_tc(const uint16_t* H, int M, int d, int64_t ldh,
   head_tc_gemm_kernel<<<grid, kTcThreads, smem, s>>>(tmW, tmH, a);
   vt_status st = launch_status("head_tc_gemm_kernel");
   if (st != VT_OK) return st;
-  rows_topk_kernel<<<M, kRowThreads, 0, s>>>(logits, V_high, k, t2f, out_ids,
-                                             out_probs);
+  RowArgs r;
+  r.logits = logits;
+  r.V_high = V_high;
+  r.k = k;
+  r.P = P;
+  r.t2f = t2f;
+  r.out_ids = out_ids;
+  r.out_probs = out_probs;
+  r.tickets = reinterpret_cast<unsigned*>(wsb + L.tickets);
+  r.part = reinterpret_cast<float*>(wsb + L.part);
+  rows_topk_kernel<<<dim3(P, M), kRowThreads, 0, s>>>(r);
   return launch_status("rows_topk_kernel");
 }
 

@@ -154,14 +154,14 @@ vt_status vt_gather_rows(const uint16_t* W, int64_t V, int32_t d,
  *   ws        (device) workspace of vt_draft_head_workspace_size(M, V_high,
  *             k) bytes.  It must be zero-filled once before its first use;
  *             the counters it holds are left zero by every call.  For
- *             M >= 5 it also holds the [M, V_high] fp32 logits (when
+ *             M >= 2 it also holds the [M, V_high] fp32 logits (when
  *             out_logits is NULL), and the 32-bit word at byte 128 is a
  *             device error word: 0, or VT_ERR_TIMEOUT if a bounded wait
  *             inside the kernel gave up (readable after a synchronise).
  *
- * Paths: M <= 4 runs a split-V GEMV (CUDA cores, one launch); M >= 5 runs a
+ * Paths: M = 1 runs a split-V GEMV (CUDA cores, one launch); M >= 2 runs a
  * tcgen05 tensor-core GEMM over all M rows at once plus a per-row softmax
- * and top-k kernel.
+ * and top-k kernel.  One workspace can serve calls of any M.
  * ------------------------------------------------------------------------ */
 size_t vt_draft_head_workspace_size(int32_t M, int32_t V_high, int32_t k);
 vt_status vt_draft_head(const uint16_t* H, int32_t M, int32_t d, int64_t ldh,

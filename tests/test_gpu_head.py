@@ -86,8 +86,8 @@ def test_head_identity_map_and_strided_H():
     run_case(1024, 3000, 2, 10, seed=5, use_t2f=False, ldh=1040)
 
 
-def test_head_many_hidden_states_grouped():
-    """M above the GEMV group size: handled four hidden states at a time."""
+def test_head_many_hidden_states():
+    """M = 9 hidden states (the tensor-core path) on a small shape."""
     run_case(512, 2000, 9, 10, seed=9)
 
 

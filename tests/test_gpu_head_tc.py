@@ -1,4 +1,4 @@
-"""GPU parity of the tree-draft (tensor-core) head path, M >= 5 hidden
+"""GPU parity of the tree-draft (tensor-core) head path, M >= 2 hidden
 states, against the CPU oracle through the C ABI: logits within
 1e-3 * (1 + |l|), probabilities within 1e-4, top-k ids equal to the
 oracle's except where oracle logits are closer than that tolerance.  Sizes
@@ -48,7 +48,8 @@ def run_tc(d, V_high, M, k, seed, rows=None, use_t2f=True, want_logits=True,
 
 
 @pytest.mark.parametrize("d,V_high,M,k", [
-    (256, 1024, 5, 8),       # smallest M on this path: N = 16
+    (256, 1024, 2, 8),       # smallest M on this path: N = 16
+    (256, 1024, 5, 8),
     (1032, 3001, 16, 10),    # ragged K block and ragged last tile
     (2048, 4096, 33, 10),    # N = 48
     (520, 777, 64, 1),       # greedy, one partial tile only
@@ -99,3 +100,24 @@ def test_tc_full_vocab_m60_sampled():
 def test_tc_qwen_and_llama1b_batch_sweep(shape, M):
     run_tc(shape.d, shape.V_high, M, shape.k, seed=shape.seed + M,
            rows=[0, M // 2, M - 1], want_logits=False)
+
+
+def test_gemv_and_tc_paths_share_one_workspace():
+    """One workspace serves calls of any M: the small-M and tree-draft paths
+    keep their counters in separate parts of the shared header, so
+    alternating them (the order that once left stale counters) stays exact."""
+    dev = need_cuda()
+    V_high, d, k = 6000, 1024, 10
+    W = synth.normal_bf16((V_high, d), 0.02, seed=41, device=dev)
+    Hs = {M: synth.normal_bf16((M, d), 1.0, seed=42 + M, device=dev)
+          for M in (1, 9, 3, 40)}
+    nbytes = max(vt.workspace_bytes("head", M=M, k=k, V_high=V_high) for M in Hs)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+    Wh = bits_host(W)
+    for M in (1, 9, 3, 40, 1, 9):
+        ids, probs = vt.draft_head(Hs[M], W, None, k, ws=ws)
+        torch.cuda.synchronize()
+        Hh = bits_host(Hs[M])
+        ref = oracle.draft_head(Hh, Wh, None, k)
+        check_topk(ids.cpu().numpy(), probs.cpu().numpy(),
+                   oracle.head_logits(Hh, Wh), None, ref, k)
