@@ -38,10 +38,11 @@ sys.path.insert(0, ROOT)
 METRIC = ("trimmed-head calls/s at d=4096 V_high=32k M=1; "
           "achieved HBM GB/s vs peak")
 WORKLOAD = "llama3-8b drafter head d=4096 V=128256 V_high=32768 M=1 top-k=10"
-HEAD_KERNEL_SRC = os.path.join(ROOT, "frequency_ranked_drafter_gb300", "csrc",
-                               "head_gemv.cu")
-PROFILE_TRAFFIC = os.path.join(ROOT, "profiles",
-                               "head_gemv_llama8b_m1_traffic.txt")
+CSRC = os.path.join(ROOT, "frequency_ranked_drafter_gb300", "csrc")
+# the sources the M = 1 head kernel is built from
+HEAD_KERNEL_SRCS = [os.path.join(CSRC, f) for f in
+                    ("head_gemv.cu", "head_common.cuh", "vt_common.cuh")]
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "head_gemv_llama8b_m1.md")
 
 
 def parse():
@@ -53,6 +54,16 @@ def parse():
     ap.add_argument("--no-build-bench", action="store_true",
                     help="skip the 1e9-token build measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweeps", action="store_true",
+                    help="skip the tree-draft and batch sweeps")
+    ap.add_argument("--case", choices=["head", "count", "select", "gather"],
+                    help="run one small case a few times (for profilers) and "
+                         "exit")
+    ap.add_argument("--M", type=int, default=1)
+    ap.add_argument("--d", type=int, default=4096)
+    ap.add_argument("--V_high", type=int, default=32768)
+    ap.add_argument("--n", type=int, default=100_000_000)
+    ap.add_argument("--calls", type=int, default=4)
     return ap.parse_args()
 
 
@@ -169,14 +180,26 @@ def smi_target(torch, dev) -> str:
         return vis.split(",")[dev.index] if vis else str(dev.index)
 
 
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for path in HEAD_KERNEL_SRCS:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def committed_traffic():
-    """dram bytes per launch of the head kernel from the committed ncu
-    summary, if that summary was taken on the current kernel source."""
+    """dram bytes per launch of the M = 1 head kernel from the committed ncu
+    summary, if that summary was taken on the current kernel sources."""
     try:
+        kv = {}
         with open(PROFILE_TRAFFIC) as f:
-            kv = dict(line.split(":", 1) for line in f if ":" in line)
-        src_hash = hashlib.sha256(open(HEAD_KERNEL_SRC, "rb").read()).hexdigest()
-        if kv.get("kernel_source_sha256", "").strip() != src_hash:
+            for line in f:
+                line = line.strip().strip("`").strip("-").strip()
+                if ":" in line:
+                    key, val = line.split(":", 1)
+                    kv[key.strip()] = val.strip()
+        if kv.get("kernel_source_sha256") != kernel_source_hash():
             return None
         return float(kv["dram_bytes_per_launch"])
     except (OSError, KeyError, ValueError):
@@ -186,7 +209,7 @@ def committed_traffic():
 # ------------------------------------------------------------------ timing
 
 def time_graph(torch, fn, steps: int, warmup: int, chunk: int = 100,
-               sampler=None):
+               sampler=None):  # noqa: C901
     """Capture `chunk` calls of fn(i) in a CUDA graph; run `warmup` calls,
     then exactly `steps` timed calls.  Returns seconds for the timed part."""
     stream = torch.cuda.current_stream()
@@ -405,6 +428,9 @@ def run_ours(args, world, rank, local):
     }
     del W_highs
 
+    if not args.no_sweeps:
+        out.update(bench_head_sweeps(torch, vt, synth, dev, W, peak))
+
     if not args.no_build_bench:
         out["build"] = bench_build(torch, vt, synth, dev, W, peak, world)
 
@@ -416,6 +442,77 @@ def run_ours(args, world, rank, local):
                       f"one host core, scaled to {V_high} rows per call"}
     if rank == 0:
         print(json.dumps(out), flush=True)
+
+
+def bench_head_sweeps(torch, vt, synth, dev, W, peak):
+    """Tree drafts (M = 60, V_high sweep) and batch sweeps (Qwen-2-7B and
+    Llama-3.2-1B shaped heads): microseconds per call, HBM and tensor
+    throughput.  Weights are slices / fresh draws of the same distribution;
+    each shape is timed over a CUDA graph of calls."""
+    out = {"tree_m60_d4096": {}, "batch_sweep": {}}
+    k = 10
+
+    def per_call(H, Wm, calls=40):
+        M = H.shape[0]
+        Vh = Wm.shape[0]
+        ids = torch.empty(M, k, dtype=torch.int32, device=dev)
+        probs = torch.empty(M, k, dtype=torch.float32, device=dev)
+        ws = torch.zeros(vt.workspace_bytes("head", M=M, k=k, V_high=Vh),
+                         dtype=torch.uint8, device=dev)
+        secs, _ = time_graph(torch, lambda i: vt.draft_head(
+            H, Wm, None, k, out_ids=ids, out_probs=probs, ws=ws), calls, 6,
+            chunk=calls)
+        return secs / calls
+
+    H60 = synth.normal_bf16((60, 4096), 1.0, seed=1013, device=dev)
+    for Vh in synth.TREE_V_HIGH_SWEEP:
+        t = per_call(H60, W[:Vh])
+        b = Vh * 4096 * 2
+        out["tree_m60_d4096"][str(Vh)] = {
+            "us_per_call": t * 1e6, "hbm_gbs": b / t / 1e9,
+            "hbm_frac": b / t / 1e9 / peak,
+            "tflops": 2 * 60 * Vh * 4096 / t / 1e12}
+    for shape in (synth.QWEN7B_HEAD, synth.LLAMA1B_HEAD):
+        Wm = synth.normal_bf16((shape.V_high, shape.d), 0.02, seed=shape.seed,
+                               device=dev)
+        row = {}
+        for M in synth.M_SWEEP:
+            H = synth.normal_bf16((M, shape.d), 1.0, seed=shape.seed + M,
+                                  device=dev)
+            t = per_call(H, Wm)
+            b = shape.V_high * shape.d * 2
+            row[str(M)] = {"us_per_call": t * 1e6, "hbm_gbs": b / t / 1e9,
+                           "hbm_frac": b / t / 1e9 / peak}
+        out["batch_sweep"][f"d={shape.d} V={shape.V} V_high={shape.V_high}"] = row
+        del Wm
+    return out
+
+
+def run_case(args):
+    """One small case, a few calls, for profilers (no timing printed)."""
+    import torch
+    import frequency_ranked_drafter_gb300 as vt
+    import synth
+    dev = torch.device("cuda", 0)
+    vt.load()
+    if args.case == "head":
+        W = synth.normal_bf16((args.V_high, args.d), 0.02, seed=5, device=dev)
+        H = synth.normal_bf16((args.M, args.d), 1.0, seed=6, device=dev)
+        for _ in range(args.calls):
+            vt.draft_head(H, W, None, 10)
+    elif args.case in ("count", "select"):
+        tokens = synth.zipf_tokens(args.n, 128256, 1.1, 1005, device=dev)
+        for _ in range(args.calls):
+            counts, _ = vt.count_tokens(tokens, 128256)
+            vt.select_vocab(counts, args.V_high)
+    elif args.case == "gather":
+        W = synth.normal_bf16((128256, args.d), 0.02, seed=5, device=dev)
+        t2f = synth.expected_rank_ids(128256, args.V_high, 1005).to(dev)
+        out = torch.empty(args.V_high, args.d, dtype=torch.bfloat16, device=dev)
+        for _ in range(args.calls):
+            vt.gather_rows(W, t2f, out=out)
+    torch.cuda.synchronize()
+    print("ok")
 
 
 def bench_build(torch, vt, synth, dev, W, peak, world):
@@ -474,6 +571,9 @@ def bench_build(torch, vt, synth, dev, W, peak, world):
 
 def main():
     args = parse()
+    if args.case:
+        run_case(args)
+        return
     world, rank, local = dist_init()
     if args.impl == "reference":
         run_reference(args, world, rank)
