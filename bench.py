@@ -253,6 +253,29 @@ def time_graph(torch, fn, steps: int, warmup: int, chunk: int = 100,
     return start.elapsed_time(end) / 1e3, clocks
 
 
+def graph_seconds(torch, fn, n: int, reps: int = 3):
+    """Seconds per call of fn, replayed n at a time from a CUDA graph
+    (best of `reps` replays)."""
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(n):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    best = float("inf")
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(
+            enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        b.synchronize()
+        best = min(best, a.elapsed_time(b) / 1e3 / n)
+    return best
+
+
 def time_events(torch, fn, reps: int, warmup: int = 2):
     for _ in range(warmup):
         fn()
@@ -540,15 +563,19 @@ def bench_build(torch, vt, synth, dev, W, peak, world):
         count_only()
         select_only()
 
-    t_count = max_over_ranks(time_events(torch, count_only, 5), world)
-    t_select = max_over_ranks(time_events(torch, select_only, 20), world)
-    t_both = max_over_ranks(time_events(torch, both, 5), world)
+    # GPU time of each stage, replayed from a CUDA graph (the stages are a
+    # fixed pipeline of launches; eager launching adds host latency that
+    # dominates the short selection kernels)
+    t_count = max_over_ranks(graph_seconds(torch, count_only, 3), world)
+    t_select = max_over_ranks(graph_seconds(torch, select_only, 20), world)
+    t_both = max_over_ranks(graph_seconds(torch, both, 3), world)
+    t_both_eager = max_over_ranks(time_events(torch, both, 3), world)
     cov = vt.coverage(sums)
     tok_bytes = cfg.n_tokens * 4
     del tokens
     W_high = torch.empty(cfg.V_high, cfg.d, dtype=torch.bfloat16, device=dev)
     t_gather = max_over_ranks(
-        time_events(torch, lambda: vt.gather_rows(W, t2f, out=W_high), 10),
+        graph_seconds(torch, lambda: vt.gather_rows(W, t2f, out=W_high), 10),
         world)
     g_bytes = 2 * cfg.V_high * cfg.d * 2
     hs_bytes = tok_bytes + cfg.V * 4 * 2
@@ -558,6 +585,8 @@ def bench_build(torch, vt, synth, dev, W, peak, world):
         "histogram_ms": t_count * 1e3,
         "select_ms": t_select * 1e3,
         "histogram_select_ms": t_both * 1e3,
+        "histogram_select_eager_ms": t_both_eager * 1e3,
+        "timing": "CUDA graph replay per stage (eager launch time also given)",
         "tokens_per_s": world * cfg.n_tokens / t_both,
         "histogram_select_gbs": hs_bytes / t_both / 1e9,
         "histogram_select_frac": hs_bytes / t_both / 1e9 / peak,

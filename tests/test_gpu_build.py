@@ -109,6 +109,8 @@ def test_select_tiny_pipeline():
     (5000, 1, 3, 4),                 # single kept id, ties at the top
     (1, 1, 10, 5),                   # one-element vocabulary
     (10000, 777, 0, 6),              # all counts zero: ids in order
+    (131072, 65536, 300, 7),         # V_high = V / 2, many tiles
+    (200000, 32768, 3000, 8),        # V above the Llama-3 vocabulary
 ])
 def test_select_cases(V, V_high, hi, seed):
     rng = np.random.default_rng(seed)
