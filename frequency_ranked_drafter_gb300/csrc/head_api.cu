@@ -5,8 +5,7 @@ extern "C" size_t vt_draft_head_workspace_size(int32_t M, int32_t V_high,
                                                int32_t k) {
   if (M <= 0 || V_high <= 0 || k <= 0) return 0;
   if (M >= vt::kHeadTcMinM) return vt::head_tc_workspace(M, V_high, k);
-  return (size_t)vt::kHeadTicketBytes +
-         (size_t)vt::kHeadMaxCtas * M * vt::head_pstride(k) * sizeof(float);
+  return vt::head_gemv_workspace(M, k);
 }
 
 extern "C" vt_status vt_draft_head(const uint16_t* H, int32_t M, int32_t d,
@@ -52,6 +51,7 @@ extern "C" vt_status vt_draft_head(const uint16_t* H, int32_t M, int32_t d,
   a.k = k;
   a.pstride = head_pstride(k);
   a.ticket = static_cast<unsigned*>(ws);
+  a.err = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + 128);
   a.part = reinterpret_cast<float*>(static_cast<char*>(ws) + kHeadTicketBytes);
   // A few hidden states: the GEMV path.
   for (int m0 = 0; m0 < M; m0 += 4) {

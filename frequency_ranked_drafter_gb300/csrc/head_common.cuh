@@ -6,6 +6,7 @@
 #include <float.h>
 #include <limits.h>
 
+#include "tc_ptx.cuh"
 #include "vt_common.cuh"
 
 namespace vt {
@@ -13,17 +14,19 @@ namespace vt {
 constexpr int kTopKMax = 32;
 constexpr int kHeadMaxCtas = 1024;
 // Workspace header shared by both head paths, so one workspace can serve
-// calls of any M: bytes [0, 8) GEMV counters, [128, 132) tensor-core path
-// error word, [1024, 2048) tensor-core per-row counters (M <= 256).  Every
+// calls of any M: bytes [0, 8) GEMV counters, [128, 132) device error word
+// (both paths), [1024, 2048) tensor-core per-row counters (M <= 256).  Every
 // counter is zero between calls; nothing else is written in the header.
 constexpr int kHeadTicketBytes = 2048;
 constexpr int kHeadRowTicketOffset = 1024;
 constexpr int kStageBytesMax = 96 * 1024;  // staged candidates, last CTA
 
-// Each CTA publishes, per hidden state m, `pstride` 32-bit words:
+// Each CTA b publishes, per hidden state m, one record of `pstride` 32-bit
+// words at part + (m * G + b) * pstride (G CTAs), 16-byte aligned so that
+// the records of one m are a single bulk copy:
 //   [0] max logit of its rows, [1] sum of exp(logit - max) over its rows,
-//   [2, 2+k) its k best logits (descending), [2+k, 2+2k) their trimmed
-//   indices (int bits); unused slots hold (-inf, INT_MAX).
+//   [2, 4) unused, [4, 4+2k) its k best entries as 64-bit keys of (logit,
+//   full-vocabulary id) (make_key), best first; unused slots kEmptyKey.
 struct HeadArgs {
   const uint16_t* H;
   int64_t ldh;
@@ -36,12 +39,20 @@ struct HeadArgs {
   int32_t* out_ids;    // [M, k]
   float* out_probs;    // [M, k]
   float* out_logits;   // [M, V_high] or null
-  float* part;         // [grid][M][pstride]
+  float* part;         // [M][grid][pstride]
   int pstride;
   unsigned* ticket;      // [0]: CTAs done; [1]: next dynamically dealt row group
+  unsigned* err;         // device error word (VT_ERR_TIMEOUT if a wait gave up)
 };
 
-inline int head_pstride(int k) { return 2 + 2 * k; }
+inline int head_pstride(int k) { return (4 + 2 * k + 3) / 4 * 4; }
+
+// Workspace of one GEMV launch over MR hidden states: the shared header and
+// up to kHeadMaxCtas CTAs' partials.
+inline size_t head_gemv_workspace(int MR, int k) {
+  return (size_t)kHeadTicketBytes +
+         (size_t)kHeadMaxCtas * MR * head_pstride(k) * sizeof(float);
+}
 
 // Arrival on a grid-wide ticket: atomic increment with acquire-release
 // semantics at gpu scope; returns the previous count.
@@ -110,149 +121,253 @@ __device__ __forceinline__ unsigned float_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Shared-memory scratch of head_final_merge (8 warps).
-struct MergeScratch {
-  float w_val[8 * kTopKMax];  // level-1 winners of each warp
-  int w_idx[8 * kTopKMax];
-  float w_max[8];
-  float w_sum[8];
+// Inverse of float_key (-0 comes back as +0).
+__device__ __forceinline__ float key_float(unsigned u) {
+  return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
+}
+
+// One 64-bit key per (logit, id) entry: larger logit first, then lower id
+// (the GEMV path keys full-vocabulary ids, so its ties fall exactly as the
+// oracle's).  Distinct ids give distinct keys; an empty slot (-inf,
+// INT_MAX) is kEmptyKey, below every real entry.
+typedef unsigned long long entry_key;
+__device__ __forceinline__ entry_key make_key(float v, int i) {
+  return ((entry_key)float_key(v) << 32) | (unsigned)~i;
+}
+__device__ __forceinline__ float key_logit(entry_key x) {
+  return key_float((unsigned)(x >> 32));
+}
+__device__ __forceinline__ int key_id(entry_key x) { return ~(int)(unsigned)x; }
+constexpr entry_key kEmptyKey = 0x007fffff80000000ull;
+
+// Double-buffered hand-over slots of cta_merge_lists for W <= 16 warps.
+constexpr int kMergeMaxWarps = 16;
+struct ListSlots {
+  entry_key key[2][kMergeMaxWarps / 2][32];
+  int val[2][kMergeMaxWarps / 2][32];
 };
 
+// Merges the sorted 32-entry lists (best first, lane j holds the j-th) that
+// the W warps of the CTA hold in (x, y) into warp 0, which ends with the 32
+// best of all of them, sorted.  Per level, the upper half of the remaining
+// warps hands its lists over through shared memory; each lower warp takes
+// max(own[j], other[31 - j]) -- the 32 best of both as a bitonic sequence --
+// and sorts it with five compare-exchange stages.  One barrier per level;
+// `level` counts levels across calls so the slots alternate.  Every thread
+// of the CTA must call it.
+template <int W, bool kPayload>
+__device__ __forceinline__ void cta_merge_lists(entry_key& x, int& y, ListSlots& ls,
+                                                int& level) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int half = W / 2; half >= 1; half >>= 1, ++level) {
+    const int buf = level & 1;
+    if (warp >= half && warp < 2 * half) {
+      ls.key[buf][warp - half][lane] = x;
+      if (kPayload) ls.val[buf][warp - half][lane] = y;
+    }
+    __syncthreads();
+    if (warp < half) {
+      const entry_key ox = ls.key[buf][warp][31 - lane];
+      if (ox > x) {
+        x = ox;
+        if (kPayload) y = ls.val[buf][warp][31 - lane];
+      }
+#pragma unroll
+      for (int st = 16; st > 0; st >>= 1) {
+        const entry_key px = __shfl_xor_sync(~0u, x, st);
+        const int py = kPayload ? __shfl_xor_sync(~0u, y, st) : 0;
+        if (((lane & st) == 0) ? (px > x) : (x > px)) {
+          x = px;
+          if (kPayload) y = py;
+        }
+      }
+    }
+  }
+}
+
+// Shared-memory scratch of head_final_merge.
+struct MergeScratch {
+  ListSlots slots;
+  entry_key surv[kTopKMax * kTopKMax];  // entries reaching the k-th head
+  int q_list[kTopKMax];                 // the lists with the k best heads
+  float w_max[kMergeMaxWarps];
+  float w_sum[kMergeMaxWarps];
+  entry_key t_key;                      // the k-th best head
+  int cnt;
+};
+
+// Bitonic sort, descending, of the 32*E keys a warp holds E per lane
+// (element i = lane + 32*r sits in register r); y rides along with its key.
+template <int E>
+__device__ __forceinline__ void warp_bitonic_desc(entry_key (&x)[E], int (&y)[E]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int size = 2; size <= 32 * E; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+#pragma unroll
+      for (int r = 0; r < E; ++r) {
+        const int i = lane + 32 * r;
+        // the lower element of a pair keeps the larger key in descending runs
+        const bool desc = (i & size) == 0;
+        if (stride >= 32) {  // partner in another register of this lane
+          const int rp = r ^ (stride >> 5);
+          if (r < rp && desc != (x[r] > x[rp])) {
+            const entry_key tx = x[r]; x[r] = x[rp]; x[rp] = tx;
+            const int ty = y[r]; y[r] = y[rp]; y[rp] = ty;
+          }
+        } else {
+          const entry_key px = __shfl_xor_sync(~0u, x[r], stride);
+          const int py = __shfl_xor_sync(~0u, y[r], stride);
+          const bool lower = (i & stride) == 0;
+          if ((desc == lower) != (x[r] > px)) {
+            x[r] = px;
+            y[r] = py;
+          }
+        }
+      }
+    }
+  }
+}
+
+// The 32 best list heads (list(b)[0]) of one warp's share b0 .. b1-1,
+// sorted, one per lane, with their list numbers; empty slots are
+// (kEmptyKey, -1).
+template <int E, class List>
+__device__ __forceinline__ void warp_top_heads(const List& list, int b0, int b1,
+                                               entry_key& ox, int& oy) {
+  const int lane = threadIdx.x & 31;
+  entry_key x[E];
+  int y[E];
+#pragma unroll
+  for (int r = 0; r < E; ++r) {
+    const int b = b0 + lane + 32 * r;
+    x[r] = b < b1 ? list(b)[0] : kEmptyKey;
+    y[r] = b < b1 ? b : -1;
+  }
+  warp_bitonic_desc<E>(x, y);
+  ox = x[0];
+  oy = y[0];
+}
+
 // Merge of all CTAs' partial results, run by the last CTA of a launch
-// (NT = 256 threads, 8 warps).  For every hidden state m:
+// (NT threads, W = NT/32 warps).  Each CTA published (max, sumexp) and its
+// k best entries as sorted keys, so for every hidden state m:
 //   Mg = max_b max_b;  Sg = sum_b sumexp_b * exp(max_b - Mg);
-//   level 1: warp w merges lists [w*L, (w+1)*L) (L = ceil(G/8), at most
-//            four lists per lane, their heads in registers) by a k-round
-//            tournament; a round is a warp arg-max done with two redux.sync
-//            (max of the order-preserving logit key, then min of the index
-//            among the lanes holding it), after which the winning list
-//            advances;
-//   level 2: the 8*k level-1 winners are ranked by counting and the k best
-//            written out by k threads at once (remap, exp, divide).
-// All partials are read in one batch of independent loads (one L2 round
-// trip) and the lists staged in shared memory (`stage`, G*k*8 bytes): this
-// part runs on one SM while the others idle.  Its cost does not depend on
-// the data.
+//   the top-k lies in the k lists whose heads are best (a list whose head
+//   is beaten by k other heads holds nothing that k entries do not beat),
+//   and within them in the entries at least as good as T, the k-th best
+//   head: at most k*k survivors.  Each warp bitonic-sorts the heads of its
+//   share of the lists in registers, the warps' sorted heads are merged in
+//   registers (cta_merge_lists) to give the k best lists and T, and the
+//   survivors are ranked by counting; the k best write their id and
+//   exp(l - Mg) / Sg.
+// The G records of one m are contiguous and reach shared memory (`stage`,
+// G * pstride words, 16-byte aligned) in one bulk copy -- one L2 round trip
+// without a load per entry; this part runs on one SM while the others idle.
+// The work does not depend on the data.  If the copy does not land within
+// the wait budget the error word is set and the merge gives up.
 template <int NT>
-__device__ void head_final_merge(const HeadArgs& a, int MR, int G,
-                                 float* stage, MergeScratch& sc) {
-  static_assert(NT == 256, "merge layout assumes 8 warps");
-  constexpr int kPer = kHeadMaxCtas / NT;      // CTA summaries per thread
-  constexpr int kBatch = 16;                   // candidates per thread per batch
-  constexpr int kOwn = kHeadMaxCtas / 8 / 32;  // lists per lane (level 1)
+__device__ void head_final_merge(const HeadArgs& a, int MR, int G, float* stage,
+                                 MergeScratch& sc, uint64_t* bar) {
+  constexpr int W = NT / 32;
+  static_assert(W >= 8 && W <= kMergeMaxWarps, "merge layout: 8 to 16 warps");
+  constexpr int kPer = kHeadMaxCtas / NT;  // CTA records per thread
+  constexpr int kSortE = kHeadMaxCtas / W / 32;  // heads per lane, <= 4
+  constexpr long long kWaitBudget = 1ll << 31;   // SM cycles, about a second
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int k = a.k, ps = a.pstride, nc = G * k;
-  float* sv = stage;
-  int* si = reinterpret_cast<int*>(stage + nc);
+  const int k = a.k, ps = a.pstride;
+  const uint32_t bytes = (uint32_t)G * ps * sizeof(float);
+  int level = 0;
+  auto list = [&](int b) {
+    return reinterpret_cast<const entry_key*>(stage + (size_t)b * ps + 4);
+  };
+  if (tid == 0) {
+    tc::mbar_init(bar, 1);
+    tc::fence_barrier_init();
+  }
+  __syncthreads();
   for (int m = 0; m < MR; ++m) {
-    auto slot = [&](int b) { return a.part + ((size_t)b * MR + m) * ps; };
-    float bm[kPer], bs[kPer];
+    if (tid == 0) {
+      // the other CTAs' records were acquired through the ticket (generic
+      // proxy); earlier generic use of `stage` is done (barrier above)
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc::mbar_arrive_expect_tx(bar, bytes);
+      asm volatile(
+          "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes"
+          " [%0], [%1], %2, [%3];" ::"r"(tc::smem_u32(stage)),
+          "l"(a.part + (size_t)m * G * ps), "r"(bytes), "r"(tc::smem_u32(bar))
+          : "memory");
+      sc.cnt = 0;
+    }
+    if (!tc::mbar_wait(bar, m & 1, kWaitBudget)) {
+      if (tid == 0) atomicExch(a.err, (unsigned)VT_ERR_TIMEOUT);
+      tc::mbar_wait(bar, m & 1, kWaitBudget);  // let the copy finish
+      return;
+    }
+    float2 st[kPer];  // this thread's CTA records' (max, sumexp)
+    float lm = -INFINITY;
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
       const int b = tid + j * NT;
-      bm[j] = b < G ? __ldcg(slot(b)) : -INFINITY;
-      bs[j] = b < G ? __ldcg(slot(b) + 1) : 0.f;
+      st[j] = b < G ? *reinterpret_cast<const float2*>(stage + (size_t)b * ps)
+                    : make_float2(-INFINITY, 0.f);
+      lm = fmaxf(lm, st[j].x);
     }
-    for (int base = 0; base < nc; base += NT * kBatch) {
-      float cv[kBatch];
-      int ci[kBatch];
 #pragma unroll
-      for (int j = 0; j < kBatch; ++j) {
-        const int c = base + j * NT + tid;
-        if (c < nc) {
-          const int b = c / k, r = c - b * k;
-          cv[j] = __ldcg(slot(b) + 2 + r);
-          ci[j] = __ldcg(reinterpret_cast<const int*>(slot(b)) + 2 + k + r);
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < kBatch; ++j) {
-        const int c = base + j * NT + tid;
-        if (c < nc) { sv[c] = cv[j]; si[c] = ci[j]; }
-      }
+    for (int o = 16; o > 0; o >>= 1) lm = fmaxf(lm, __shfl_xor_sync(~0u, lm, o));
+    if (lane == 0) sc.w_max[warp] = lm;
+    entry_key hx;
+    int hy;
+    {
+      const int L = (G + W - 1) / W;
+      const int b0 = warp * L, b1 = min(G, b0 + L);
+      if (L <= 32) warp_top_heads<1>(list, b0, b1, hx, hy);
+      else if (L <= 64) warp_top_heads<2>(list, b0, b1, hx, hy);
+      else warp_top_heads<kSortE>(list, b0, b1, hx, hy);
     }
-    float wm = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) wm = fmaxf(wm, bm[j]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(~0u, wm, o));
-    if (lane == 0) sc.w_max[warp] = wm;
-    __syncthreads();  // publishes the stage and the warp maxima
+    // the k best heads of all, in order (distinct: lists hold disjoint ids);
+    // the first barrier inside also publishes the warp maxima
+    cta_merge_lists<W, true>(hx, hy, sc.slots, level);
+    if (warp == 0 && lane < k) {
+      sc.q_list[lane] = hy;
+      if (lane == k - 1) sc.t_key = hx;
+    }
+    __syncthreads();
+    const entry_key t = sc.t_key;
+    for (int c = tid; c < k * k; c += NT) {
+      const int j = c / k;
+      const int b = sc.q_list[j];
+      if (b < 0) continue;
+      const entry_key x = list(b)[c - j * k];
+      if (x >= t && x != kEmptyKey) sc.surv[atomicAdd(&sc.cnt, 1)] = x;
+    }
     float mg = sc.w_max[0];
 #pragma unroll
-    for (int w = 1; w < 8; ++w) mg = fmaxf(mg, sc.w_max[w]);
+    for (int w = 1; w < W; ++w) mg = fmaxf(mg, sc.w_max[w]);
     float ws = 0.f;
 #pragma unroll
     for (int j = 0; j < kPer; ++j)
-      if (bs[j] > 0.f) ws += bs[j] * __expf(bm[j] - mg);
+      if (st[j].y > 0.f) ws += st[j].y * __expf(st[j].x - mg);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(~0u, ws, o);
     if (lane == 0) sc.w_sum[warp] = ws;
-
-    // ---- level 1: per-warp tournament over its lists
-    {
-      const int L = (G + 7) / 8;
-      const int b0 = warp * L, b1 = min(G, b0 + L);
-      int hd[kOwn];
-      float hv[kOwn];
-      int hi[kOwn];
-#pragma unroll
-      for (int o = 0; o < kOwn; ++o) {
-        const int b = b0 + lane + 32 * o;
-        hd[o] = 0;
-        hv[o] = b < b1 ? sv[b * k] : -INFINITY;
-        hi[o] = b < b1 ? si[b * k] : INT_MAX;
-      }
-      float rv = -INFINITY;
-      int ri = INT_MAX;
-      for (int r = 0; r < k; ++r) {
-        float lv = -INFINITY;
-        int li = INT_MAX, lo = 0;
-#pragma unroll
-        for (int o = 0; o < kOwn; ++o)
-          if (hi[o] != INT_MAX && key_beats(hv[o], hi[o], lv, li)) {
-            lv = hv[o]; li = hi[o]; lo = o;
-          }
-        const unsigned lk = li != INT_MAX ? float_key(lv) : 0u;
-        const unsigned wk = __reduce_max_sync(~0u, lk);
-        if (wk == 0u) break;  // this warp's lists are exhausted
-        const int wi = (int)__reduce_min_sync(
-            ~0u, lk == wk ? (unsigned)li : 0xffffffffu);
-        const unsigned owner = __ballot_sync(~0u, lk == wk && li == wi);
-        const int ol = __ffs(owner) - 1;
-        const float wv = __shfl_sync(~0u, lv, ol);
-        if (lane == r) { rv = wv; ri = wi; }
-        if (lane == ol) {  // the winning list advances
-#pragma unroll
-          for (int o = 0; o < kOwn; ++o)
-            if (o == lo) {
-              const int b = b0 + lane + 32 * o;
-              const int h = ++hd[o];
-              hv[o] = h < k ? sv[b * k + h] : -INFINITY;
-              hi[o] = h < k ? si[b * k + h] : INT_MAX;
-            }
-        }
-      }
-      if (lane < k) { sc.w_val[warp * k + lane] = rv; sc.w_idx[warp * k + lane] = ri; }
-    }
     __syncthreads();
-
-    // ---- level 2: rank the 8*k level-1 winners, write the k best
     float sg = 0.f;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) sg += sc.w_sum[w];
+    for (int w = 0; w < W; ++w) sg += sc.w_sum[w];
+    const int S = sc.cnt;
     int32_t* ids = a.out_ids + (size_t)m * k;
     float* probs = a.out_probs + (size_t)m * k;
-    for (int c = tid; c < 8 * k; c += NT) {
-      const float v = sc.w_val[c];
-      const int i = sc.w_idx[c];
-      if (i == INT_MAX) continue;
+    for (int c = tid; c < S; c += NT) {
+      const entry_key x = sc.surv[c];
       int rank = 0;
-      for (int q = 0; q < 8 * k; ++q)
-        rank += key_beats(sc.w_val[q], sc.w_idx[q], v, i);
+      for (int q = 0; q < S; ++q) rank += sc.surv[q] > x;
       if (rank < k) {
-        ids[rank] = a.t2f ? a.t2f[i] : i;
-        probs[rank] = expf(v - mg) / sg;
+        ids[rank] = key_id(x);
+        probs[rank] = expf(key_logit(x) - mg) / sg;
       }
     }
     __syncthreads();

@@ -8,12 +8,14 @@
 // softmax of the drafter logits, then trimmed index -> full id through
 // trimmed_to_full.
 //
-// At M <= 4 hidden states the head is a GEMV bound by reading W_high once
+// At one hidden state the head is a GEMV bound by reading W_high once
 // (V_high * d * 2 bytes).  One launch does everything:
-//   * every warp of the grid streams whole rows of W_high with 16-byte
-//     loads (up to 16 per lane in flight) and dots them with H, which each
-//     CTA keeps in shared memory as fp32; rows are dealt round-robin over all
-//     warps of the grid, so every SM streams the same number of bytes;
+//   * two CTAs of 8 warps per SM; every warp streams whole rows of W_high
+//     with 16-byte loads (up to 16 per lane in flight) and dots them with H,
+//     which each CTA keeps in shared memory as fp32; most rows are dealt
+//     round-robin over all warps of the grid and the last eighth one group
+//     at a time from a counter, so every SM streams about the same bytes
+//     and all finish together;
 //   * each warp keeps, per hidden state, an online (max, sum of exp) and a
 //     sorted top-k list held one entry per lane (insertion by ballot and a
 //     one-lane shift), so no logit is ever written to memory;
@@ -54,10 +56,9 @@ template <int MR, int CPL, int U>
 __global__ void __launch_bounds__(kGemvThreads, 2)
     head_gemv_kernel(HeadArgs a) {
   extern __shared__ __align__(16) float hs[];  // [MR][d] fp32 hidden states
-  __shared__ float c_val[MR][kGemvWarps * kTopKMax];
-  __shared__ int c_idx[MR][kGemvWarps * kTopKMax];
   __shared__ float w_mx[MR][kGemvWarps], w_se[MR][kGemvWarps];
   __shared__ MergeScratch msc;
+  __shared__ uint64_t merge_bar;
   __shared__ int s_last;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -75,12 +76,14 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
   }
   __syncthreads();
 
-  float mx[MR], se[MR], tv[MR], thr[MR];
-  int ti[MR];
+  // Per hidden state: running max and sum of exp (online softmax), and the
+  // warp's k best entries as keys of (logit, full-vocabulary id), lane j
+  // holding the j-th best, with thr the k-th.
+  float mx[MR], se[MR];
+  entry_key tk[MR], thr[MR];
 #pragma unroll
   for (int m = 0; m < MR; ++m) {
-    mx[m] = -INFINITY; se[m] = 0.f; tv[m] = -INFINITY; thr[m] = -INFINITY;
-    ti[m] = INT_MAX;
+    mx[m] = -INFINITY; se[m] = 0.f; tk[m] = kEmptyKey; thr[m] = kEmptyKey;
   }
 
   const int nchunks = d >> 3;
@@ -92,6 +95,13 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
 
   auto process_group = [&](int g) {
     const int r0 = g * U;
+    // full ids of the group's rows, fetched while the rows stream in
+    int fid[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int row = min(r0 + u, a.V_high - 1);
+      fid[u] = a.t2f ? __ldg(a.t2f + row) : row;
+    }
     float acc[U][MR];
 #pragma unroll
     for (int u = 0; u < U; ++u)
@@ -141,15 +151,13 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
         } else {
           se[m] += __expf(l - mx[m]);
         }
-        // rows grow along a warp's walk, so an equal logit never displaces
-        if (l > thr[m]) {
-          const unsigned ahead = __ballot_sync(~0u, lane < k && tv[m] >= l);
-          const int p = __popc(ahead);
-          const float up_v = __shfl_up_sync(~0u, tv[m], 1);
-          const int up_i = __shfl_up_sync(~0u, ti[m], 1);
-          if (lane == p) { tv[m] = l; ti[m] = row; }
-          else if (lane > p && lane < k) { tv[m] = up_v; ti[m] = up_i; }
-          thr[m] = __shfl_sync(~0u, tv[m], k - 1);
+        const entry_key key = make_key(l, fid[u]);
+        if (key > thr[m]) {  // insert at its rank, the k-th drops out
+          const int p = __popc(__ballot_sync(~0u, lane < k && tk[m] > key));
+          const entry_key up = __shfl_up_sync(~0u, tk[m], 1);
+          if (lane == p) tk[m] = key;
+          else if (lane > p && lane < k) tk[m] = up;
+          thr[m] = __shfl_sync(~0u, tk[m], k - 1);
         }
       }
     }
@@ -174,46 +182,33 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
     process_group(g);
   }
 
-  // ---- CTA merge: rank counting over the warps' lists.
+  // ---- CTA merge: the warps' sorted lists are merged in registers into
+  // warp 0 (cta_merge_lists), which publishes the k best; warp 0 also folds
+  // the warps' (max, sumexp).
+  float* rec[MR];
 #pragma unroll
   for (int m = 0; m < MR; ++m) {
-    if (lane < k) {
-      c_val[m][warp * k + lane] = tv[m];
-      c_idx[m][warp * k + lane] = ti[m];
-    }
+    rec[m] = a.part + ((size_t)m * gridDim.x + blockIdx.x) * a.pstride;
     if (lane == 0) { w_mx[m][warp] = mx[m]; w_se[m][warp] = se[m]; }
   }
-  __syncthreads();
-  const int nc = kGemvWarps * k;
-  float* part = a.part + (size_t)blockIdx.x * MR * a.pstride;
-  for (int t = tid; t < MR * a.pstride; t += kGemvThreads) {
-    // empty slots of the published list: (-inf, INT_MAX)
-    const int o = t % a.pstride;
-    if (o >= 2 && o < 2 + k) part[t] = -INFINITY;
-    else if (o >= 2 + k && o < 2 + 2 * k) reinterpret_cast<int*>(part)[t] = INT_MAX;
-  }
-  __syncthreads();
-  for (int t = tid; t < MR * nc; t += kGemvThreads) {
-    const int m = t / nc, c = t % nc;
-    const float v = c_val[m][c];
-    const int i = c_idx[m][c];
-    if (i == INT_MAX) continue;
-    int rank = 0;
-    for (int q = 0; q < nc; ++q) rank += key_beats(c_val[m][q], c_idx[m][q], v, i);
-    if (rank < k) {
-      part[m * a.pstride + 2 + rank] = v;
-      reinterpret_cast<int*>(part)[m * a.pstride + 2 + k + rank] = i;
+  int level = 0;
+#pragma unroll
+  for (int m = 0; m < MR; ++m) {
+    entry_key x = tk[m];
+    int unused = 0;
+    cta_merge_lists<kGemvWarps, false>(x, unused, msc.slots, level);
+    if (warp == 0) {
+      if (lane < k) reinterpret_cast<entry_key*>(rec[m] + 4)[lane] = x;
+      const float wmx = lane < kGemvWarps ? w_mx[m][lane] : -INFINITY;
+      const float wse = lane < kGemvWarps ? w_se[m][lane] : 0.f;
+      float M_b = wmx;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) M_b = fmaxf(M_b, __shfl_xor_sync(~0u, M_b, o));
+      float S_b = wse > 0.f ? wse * __expf(wmx - M_b) : 0.f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) S_b += __shfl_xor_sync(~0u, S_b, o);
+      if (lane == 0) { rec[m][0] = M_b; rec[m][1] = S_b; }
     }
-  }
-  if (tid < MR) {
-    const int m = tid;
-    float M_b = -INFINITY;
-    for (int w = 0; w < kGemvWarps; ++w) M_b = fmaxf(M_b, w_mx[m][w]);
-    float S_b = 0.f;
-    for (int w = 0; w < kGemvWarps; ++w)
-      if (w_se[m][w] > 0.f) S_b += w_se[m][w] * __expf(w_mx[m][w] - M_b);
-    part[m * a.pstride + 0] = M_b;
-    part[m * a.pstride + 1] = S_b;
   }
 
   // ---- last CTA merges every CTA's (max, sumexp, top-k).  The barrier
@@ -224,7 +219,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
   if (tid == 0) s_last = ticket_arrive(a.ticket) == gridDim.x - 1;
   __syncthreads();
   if (!s_last) return;
-  head_final_merge<kGemvThreads>(a, MR, gridDim.x, hs, msc);
+  head_final_merge<kGemvThreads>(a, MR, gridDim.x, hs, msc, &merge_bar);
   if (tid == 0) {
     a.ticket[0] = 0u;
     a.ticket[1] = 0u;
@@ -236,14 +231,14 @@ vt_status launch_gemv(const HeadArgs& a, const DeviceInfo& di,
                       cudaStream_t s) {
   auto kern = head_gemv_kernel<MR, CPL, U>;
   const int64_t groups = (a.V_high + U - 1) / U;
-  // Two CTAs per SM (the launch bound); no more CTAs than warps have rows,
-  // and no more than the last CTA can stage candidates of (G * k * 8 bytes).
+  // Two CTAs of 8 warps per SM (the launch bound); no more CTAs than warps
+  // have rows, and no more than the last CTA can stage records of.
   int64_t G = std::min<int64_t>((int64_t)di.num_sms * 2,
                                 (groups + kGemvWarps - 1) / kGemvWarps);
-  G = std::min<int64_t>(G, kStageBytesMax / (8 * a.k));
+  G = std::min<int64_t>(G, kStageBytesMax / (a.pstride * (int64_t)sizeof(float)));
   G = std::max<int64_t>(1, std::min<int64_t>(G, kHeadMaxCtas));
   const int smem = (int)std::max<int64_t>((int64_t)MR * a.d * sizeof(float),
-                                          G * a.k * 8);
+                                          G * a.pstride * (int64_t)sizeof(float));
   if (smem > di.max_smem_optin)
     return fail(VT_ERR_UNSUPPORTED, "head_gemv: M * d too large for smem");
   if (!allow_max_smem(kern, di)) return VT_ERR_CUDA;

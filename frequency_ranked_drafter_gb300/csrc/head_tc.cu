@@ -21,7 +21,9 @@
 //
 // Softmax + top-k: each hidden state's V_high logits (L2-resident) are
 // split over CTAs of 4096; each CTA reduces its part to (max, sum of exp,
-// exact top-k) and the last CTA of the row merges the parts.
+// exact top-k) and the last CTA of the row merges the parts.  Entries carry
+// their full-vocabulary id (t2f read next to the logits), which breaks ties
+// between equal logits (lower id first) and is what the call returns.
 //
 // Every wait on an mbarrier is bounded (kWaitBudget cycles, about a
 // second); a wait that gives up records VT_ERR_TIMEOUT in the error word of
@@ -252,8 +254,10 @@ __global__ void __launch_bounds__(kRowThreads)
   const int base = part_idx * kRowSpan;
 
   // this thread's values: 4 float4 at base + 4*(tid + 256*q) (or scalars
-  // when the row is not 16-byte aligned or at the tail)
+  // when the row is not 16-byte aligned or at the tail), and their
+  // full-vocabulary ids, which break ties between equal logits
   float v[kRowVals];
+  int f[kRowVals];
   const bool vec = ((a.V_high & 3) == 0) &&
                    ((reinterpret_cast<uintptr_t>(a.logits) & 15) == 0);
 #pragma unroll
@@ -267,6 +271,11 @@ __global__ void __launch_bounds__(kRowThreads)
       for (int e = 0; e < 4; ++e)
         v[4 * q + e] = i0 + e < a.V_high ? __ldcg(row + i0 + e) : -INFINITY;
     }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = i0 + e;
+      f[4 * q + e] = i < a.V_high ? (a.t2f ? __ldg(a.t2f + i) : i) : INT_MAX;
+    }
   }
   auto idx_of = [&](int j) { return base + 4 * (tid + kRowThreads * (j >> 2)) + (j & 3); };
 
@@ -275,8 +284,7 @@ __global__ void __launch_bounds__(kRowThreads)
 #pragma unroll
   for (int j = 0; j < kRowVals; ++j) {
     mx = fmaxf(mx, v[j]);
-    const int i = idx_of(j);
-    if (i < a.V_high && key_beats(v[j], i, bv, bi)) { bv = v[j]; bi = i; }
+    if (idx_of(j) < a.V_high && key_beats(v[j], f[j], bv, bi)) { bv = v[j]; bi = f[j]; }
   }
   float se = 0.f;
   if (mx > -INFINITY) {
@@ -313,10 +321,9 @@ __global__ void __launch_bounds__(kRowThreads)
     }
 #pragma unroll
   for (int j = 0; j < kRowVals; ++j) {
-    const int i = idx_of(j);
-    if (i < a.V_high && !key_beats(T_v, T_i, v[j], i)) {
+    if (idx_of(j) < a.V_high && !key_beats(T_v, T_i, v[j], f[j])) {
       const int p = atomicAdd(&s_cnt, 1);
-      if (p < kRowSurvivors) surv[p] = make_float2(v[j], __int_as_float(i));
+      if (p < kRowSurvivors) surv[p] = make_float2(v[j], __int_as_float(f[j]));
     }
   }
   __syncthreads();
@@ -373,7 +380,7 @@ __global__ void __launch_bounds__(kRowThreads)
     int rank = 0;
     for (int q = 0; q < nc; ++q) rank += key_beats(surv[q].x, __float_as_int(surv[q].y), x, i);
     if (rank < k) {
-      ids[rank] = a.t2f ? a.t2f[i] : i;
+      ids[rank] = i;
       probs[rank] = expf(x - mg) / sg;
     }
   }

@@ -155,9 +155,10 @@ vt_status vt_gather_rows(const uint16_t* W, int64_t V, int32_t d,
  *             k) bytes.  It must be zero-filled once before its first use;
  *             the counters it holds are left zero by every call.  For
  *             M >= 2 it also holds the [M, V_high] fp32 logits (when
- *             out_logits is NULL), and the 32-bit word at byte 128 is a
- *             device error word: 0, or VT_ERR_TIMEOUT if a bounded wait
- *             inside the kernel gave up (readable after a synchronise).
+ *             out_logits is NULL).  On every path the 32-bit word at byte
+ *             128 is a device error word: 0, or VT_ERR_TIMEOUT if a bounded
+ *             wait inside the kernel gave up (readable after a synchronise;
+ *             the outputs of that call are then incomplete).
  *
  * Paths: M = 1 runs a split-V GEMV (CUDA cores, one launch); M >= 2 runs a
  * tcgen05 tensor-core GEMM over all M rows at once plus a per-row softmax
@@ -184,9 +185,10 @@ vt_status vt_draft_head(const uint16_t* H, int32_t M, int32_t d, int64_t ldh,
  * library defines and every GPU that loads the library keeps until exit.
  * It always runs the GEMV kernel, four hidden states at a time.
  *
- *   Limit     the scratch needed, vt_draft_head_workspace_size(min(M, 4),
- *             V_high, k), must fit in 1 MiB (any k <= 32 for M <= 3; k <= 30 for
- *             M >= 4); larger requests return VT_ERR_UNSUPPORTED.
+ *   Limit     the GEMV scratch, 2048 + 4096 * min(M, 4) * P bytes with
+ *             P = 4 + 2k rounded up to a multiple of 4, must fit in 1 MiB:
+ *             any k <= 32 for M <= 3, k <= 28 for M >= 4; larger requests
+ *             return VT_ERR_UNSUPPORTED.
  *   Set-up    the first call on each device looks up the array's device
  *             address and zero-fills its counters with a synchronous
  *             cudaMemset; make that first call before any stream capture.

@@ -28,8 +28,11 @@ def run_case(d, V_high, M, k, seed, hs=1.0, ws=0.02, use_t2f=True,
         t2f = synth.rank_permutation(V, seed)[:V_high].to(dev)
     logits = (torch.empty(M, V_high, dtype=torch.float32, device=dev)
               if want_logits else None)
-    ids, probs = vt.draft_head(H, W_high, t2f, k, out_logits=logits)
+    wsb = torch.zeros(vt.workspace_bytes("head", M=M, k=k, V_high=V_high),
+                      dtype=torch.uint8, device=dev)
+    ids, probs = vt.draft_head(H, W_high, t2f, k, out_logits=logits, ws=wsb)
     torch.cuda.synchronize()
+    assert int(wsb[128:132].view(torch.int32).item()) == 0, "device error word"
     rows = list(range(M)) if check_rows is None else check_rows
     Hh = bits_host(H[rows])
     Wh = bits_host(W_high)
@@ -97,22 +100,43 @@ def test_head_large_logits_no_overflow():
     assert torch.isfinite(probs).all()
 
 
-def test_head_uniform_logits_ties():
-    """All logits equal: probabilities are exactly 1/V_high; the GPU orders
-    equal logits by trimmed index, the oracle by full id, so only the
-    probabilities and the validity of ids are compared."""
+@pytest.mark.parametrize("M", [1, 4])
+def test_head_uniform_logits_ties(M):
+    """All logits equal: probabilities are exactly 1/V_high and, ties going
+    to the lower full-vocabulary id on both paths (as in the oracle), the
+    ids are the k lowest full ids even though t2f lists them last."""
     dev = need_cuda()
     V_high, d, k = 3000, 256, 10
     W = torch.zeros(V_high, d, dtype=torch.bfloat16, device=dev)
-    H = torch.ones(1, d, dtype=torch.bfloat16, device=dev)
+    H = torch.ones(M, d, dtype=torch.bfloat16, device=dev)
     t2f = torch.arange(V_high, dtype=torch.int32, device=dev).flip(0).contiguous()
     ids, probs = vt.draft_head(H, W, t2f, k)
     torch.testing.assert_close(probs, torch.full_like(probs, 1.0 / V_high),
                                rtol=1e-5, atol=0)
-    assert sorted(set(ids[0].tolist())) == sorted(ids[0].tolist())
-    # lowest trimmed indices first: t2f[0..k-1]
-    assert ids[0].tolist() == t2f[:k].tolist()
+    for m in range(M):
+        assert ids[m].tolist() == list(range(k))
 
+
+@pytest.mark.parametrize("M", [1, 3, 40])
+def test_head_exact_ties_match_oracle_ids(M):
+    """Logits exact in fp32 whatever the summation order (0/1 hidden states,
+    weights in {0, 1/16}) and full of ties: the ids equal the oracle's
+    exactly on the GEMV (M < 2) and tensor-core paths, probabilities within
+    1e-4."""
+    dev = need_cuda()
+    V_high, d, k = 3000, 256, 10
+    rng = np.random.default_rng(100 + M)
+    Wf = rng.integers(0, 2, size=(V_high, d)).astype(np.float32) * 0.0625
+    Hf = rng.integers(0, 2, size=(M, d)).astype(np.float32)
+    W = torch.from_numpy(Wf).to(torch.bfloat16).to(dev)
+    H = torch.from_numpy(Hf).to(torch.bfloat16).to(dev)
+    t2f = synth.rank_permutation(4 * V_high, 9)[:V_high].to(dev)
+    ids, probs = vt.draft_head(H, W, t2f, k)
+    torch.cuda.synchronize()
+    ref = oracle.draft_head(bits_host(H), bits_host(W), t2f.cpu().numpy(), k)
+    assert np.array_equal(ids.cpu().numpy(), ref["ids"])
+    np.testing.assert_allclose(probs.cpu().numpy(), ref["probs"], rtol=0,
+                               atol=1e-4)
 
 def test_head_repeated_calls_identical():
     """The workspace counters are re-armed by every call: repeated calls
