@@ -41,7 +41,8 @@ WORKLOAD = "llama3-8b drafter head d=4096 V=128256 V_high=32768 M=1 top-k=10"
 CSRC = os.path.join(ROOT, "frequency_ranked_drafter_gb300", "csrc")
 # the sources the M = 1 head kernel is built from
 HEAD_KERNEL_SRCS = [os.path.join(CSRC, f) for f in
-                    ("head_gemv.cu", "head_common.cuh", "vt_common.cuh")]
+                    ("head_gemv.cu", "head_common.cuh", "vt_common.cuh",
+                     "tc_ptx.cuh")]
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "head_gemv_llama8b_m1.md")
 
 
