@@ -61,9 +61,16 @@ def _load():
         lib.oracle_head_logits.argtypes = [p, i32, i32, i64, p, i32, p]
         lib.oracle_draft_head.argtypes = [p, i32, i32, i64, p, i32, p, i32,
                                           p, p, p, p, p, p]
+        u64, f64 = ctypes.c_uint64, ctypes.c_double
+        lib.oracle_philox4x32_10.argtypes = [p, p, p]
+        lib.oracle_gumbel_noise.argtypes = [u64, u64, i32, p, i64, p]
+        lib.oracle_draft_head_ex.argtypes = [p, i32, i32, i64, p, i32, p, p,
+                                             f64, i32, u64, u64, i32, p, p, p,
+                                             p, p, p, p]
         for fn in (lib.oracle_count_tokens, lib.oracle_select_vocab,
                    lib.oracle_gather_rows, lib.oracle_head_logits,
-                   lib.oracle_draft_head):
+                   lib.oracle_draft_head, lib.oracle_philox4x32_10,
+                   lib.oracle_gumbel_noise, lib.oracle_draft_head_ex):
             fn.restype = ctypes.c_int
         _lib = lib
         return lib
@@ -165,3 +172,58 @@ def draft_head(H, W_high, t2f, k: int):
         raise ValueError(f"oracle_draft_head: bad arguments (rc={rc})")
     return dict(ids=ids, probs=probs, logits=logits, trimmed=trimmed,
                 row_max=rmax, row_sumexp=rsum)
+
+
+def philox4x32_10(ctr, key):
+    """Philox4x32-10 output block (4 x uint32) for counter[4], key[2]."""
+    c = np.ascontiguousarray(ctr, dtype=np.uint32)
+    kk = np.ascontiguousarray(key, dtype=np.uint32)
+    out = np.empty(4, dtype=np.uint32)
+    _load().oracle_philox4x32_10(_ptr(c), _ptr(kk), _ptr(out))
+    return out
+
+
+def gumbel_noise(seed: int, offset: int, m: int, full_ids):
+    """Gumbel noise of the given full ids for hidden state m at (seed, offset)."""
+    f = np.ascontiguousarray(full_ids, dtype=np.int32)
+    out = np.empty(f.size, dtype=np.float64)
+    _load().oracle_gumbel_noise(ctypes.c_uint64(seed), ctypes.c_uint64(offset),
+                                m, _ptr(f), f.size, _ptr(out))
+    return out
+
+
+def draft_head_ex(H, W_high, t2f, k: int, bias=None, temperature=1.0,
+                  sample=False, seed=0, offset=0):
+    """Draft step with options: optional kept-row bias (fp32), temperature,
+    top-k or Gumbel-max sampling (k draws without replacement).
+
+    Returns dict with ids[M,k], probs[M,k], scores[M,k] (selection keys),
+    logits[M,k], trimmed[M,k], row_max[M] (of logit/T), row_sumexp[M].
+    """
+    H = _u16(H)
+    W_high = _u16(W_high)
+    M, d = H.shape
+    V_high = W_high.shape[0]
+    if t2f is not None:
+        t2f = np.ascontiguousarray(t2f, dtype=np.int32)
+        assert t2f.size == V_high
+    if bias is not None:
+        bias = np.ascontiguousarray(bias, dtype=np.float32)
+        assert bias.size == V_high
+    ids = np.empty((M, k), dtype=np.int32)
+    probs = np.empty((M, k), dtype=np.float64)
+    scores = np.empty((M, k), dtype=np.float64)
+    logits = np.empty((M, k), dtype=np.float64)
+    trimmed = np.empty((M, k), dtype=np.int32)
+    rmax = np.empty(M, dtype=np.float64)
+    rsum = np.empty(M, dtype=np.float64)
+    rc = _load().oracle_draft_head_ex(
+        _ptr(H), M, d, d, _ptr(W_high), V_high, _ptr(t2f), _ptr(bias),
+        ctypes.c_double(temperature), 1 if sample else 0,
+        ctypes.c_uint64(seed), ctypes.c_uint64(offset), k, _ptr(ids),
+        _ptr(probs), _ptr(scores), _ptr(logits), _ptr(trimmed), _ptr(rmax),
+        _ptr(rsum))
+    if rc:
+        raise ValueError(f"oracle_draft_head_ex: bad arguments (rc={rc})")
+    return dict(ids=ids, probs=probs, scores=scores, logits=logits,
+                trimmed=trimmed, row_max=rmax, row_sumexp=rsum)

@@ -24,7 +24,14 @@
 //     exactly V_high entries;
 //   * ids outside [0, V) are not counted; they are reported separately and do
 //     not enter the coverage denominator;
-//   * top-k ties: larger logit first, then lower full-vocabulary id.
+//   * top-k ties: larger logit first, then lower full-vocabulary id;
+//   * drawing from the trimmed distribution ([VT] Step 4 samples with
+//     multinomial) is done by the Gumbel-max rule, which draws from the same
+//     distribution: the noise of each token comes from the counter-based
+//     generator Philox4x32-10 keyed by (seed, step offset, hidden state,
+//     full-vocabulary id), so a token's noise does not depend on which other
+//     tokens were kept.  The k best of logit/T + noise are k draws without
+//     replacement (k = 1: one draw).
 //
 // Build: g++ -O2 -std=c++17 -shared -fPIC oracle.cpp -o liboracle.so
 #include <algorithm>
@@ -42,6 +49,54 @@ double bf16_to_double(uint16_t bits) {
   float f;
   std::memcpy(&f, &u, sizeof f);
   return static_cast<double>(f);
+}
+
+// Philox4x32-10: the counter-based generator of Salmon, Moraes, Dror and
+// Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3" (SC 2011).  Ten rounds;
+// a round multiplies counter words 0 and 2 by the two round multipliers
+// (64-bit products split into high and low halves) and mixes in the key;
+// the key advances by the two Weyl increments between rounds.
+void philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2],
+                   uint32_t out[4]) {
+  const uint64_t kMul0 = 0xD2511F53u, kMul1 = 0xCD9E8D57u;
+  const uint32_t kWeyl0 = 0x9E3779B9u, kWeyl1 = 0xBB67AE85u;
+  uint32_t c[4] = {ctr_in[0], ctr_in[1], ctr_in[2], ctr_in[3]};
+  uint32_t k[2] = {key_in[0], key_in[1]};
+  for (int round = 0; round < 10; ++round) {
+    if (round > 0) {
+      k[0] += kWeyl0;
+      k[1] += kWeyl1;
+    }
+    const uint64_t p0 = kMul0 * c[0];
+    const uint64_t p1 = kMul1 * c[2];
+    const uint32_t hi0 = static_cast<uint32_t>(p0 >> 32);
+    const uint32_t lo0 = static_cast<uint32_t>(p0);
+    const uint32_t hi1 = static_cast<uint32_t>(p1 >> 32);
+    const uint32_t lo1 = static_cast<uint32_t>(p1);
+    const uint32_t n0 = hi1 ^ c[1] ^ k[0];
+    const uint32_t n2 = hi0 ^ c[3] ^ k[1];
+    c[0] = n0;
+    c[1] = lo1;
+    c[2] = n2;
+    c[3] = lo0;
+  }
+  for (int i = 0; i < 4; ++i) out[i] = c[i];
+}
+
+// Gumbel noise of token `full_id` for hidden state m at step (seed, offset):
+// x = word 0 of Philox4x32-10 with counter (full_id, m, offset low, offset
+// high) and key (seed low, seed high); u = ((x >> 9) + 1/2) / 2^23, which
+// lies in (0, 1) and is exact in binary32; g = -log(-log(u)).
+double gumbel_noise(uint64_t seed, uint64_t offset, int32_t m, int32_t full_id) {
+  const uint32_t ctr[4] = {static_cast<uint32_t>(full_id), static_cast<uint32_t>(m),
+                           static_cast<uint32_t>(offset),
+                           static_cast<uint32_t>(offset >> 32)};
+  const uint32_t key[2] = {static_cast<uint32_t>(seed),
+                           static_cast<uint32_t>(seed >> 32)};
+  uint32_t x[4];
+  philox4x32_10(ctr, key, x);
+  const double u = (static_cast<double>(x[0] >> 9) + 0.5) / 8388608.0;
+  return -std::log(-std::log(u));
 }
 
 }  // namespace
@@ -188,6 +243,86 @@ int oracle_draft_head(const uint16_t* H, int32_t M, int32_t d, int64_t ldh,
       const int64_t o = static_cast<int64_t>(m) * k + r;
       if (ids) ids[o] = full_id(i);
       if (probs) probs[o] = std::exp(logits[i] - mx) / sumexp;
+      if (top_logits) top_logits[o] = logits[i];
+      if (trimmed_idx) trimmed_idx[o] = i;
+    }
+    if (row_max) row_max[m] = mx;
+    if (row_sumexp) row_sumexp[m] = sumexp;
+  }
+  return 0;
+}
+
+// Philox4x32-10 output block for one (counter, key), for the pins.
+int oracle_philox4x32_10(const uint32_t* ctr, const uint32_t* key,
+                         uint32_t* out) {
+  philox4x32_10(ctr, key, out);
+  return 0;
+}
+
+// Gumbel noise for n full ids (see gumbel_noise), for the pins.
+int oracle_gumbel_noise(uint64_t seed, uint64_t offset, int32_t m,
+                        const int32_t* full_ids, int64_t n, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = gumbel_noise(seed, offset, m, full_ids[i]);
+  return 0;
+}
+
+// One draft step with the head's options.
+//   logits   : l_i = sum_j H[m][j] * W_high[i][j] + b_i, where b = bias_high
+//              (the kept rows' bias, [VT] Step 3's optional bias copy;
+//              nullptr = no bias), every product exact in double;
+//   temper   : s_i = l_i / temperature (temperature > 0; 1 = plain logits);
+//   softmax  : p_i = exp(s_i - max s) / sum_j exp(s_j - max s), over the kept
+//              rows only, in double;
+//   select   : mode 0 (top-k): the k largest s_i; mode 1 (sample): the k
+//              largest s_i + g_i with g_i = gumbel_noise(seed, offset, m,
+//              full id of i): one draw from p for k = 1 (Gumbel-max), k
+//              draws without replacement for k > 1; ties in either key go
+//              to the lower full id; descending;
+//   remap    : trimmed index -> full id through t2f (nullptr = identity).
+// Outputs per row m (each nullable): ids[m*k+r], probs[m*k+r] = p of the
+// chosen entry, scores[m*k+r] = its selection key, top_logits[m*k+r] = its
+// l, trimmed_idx[m*k+r], row_max[m] = max s, row_sumexp[m].
+int oracle_draft_head_ex(const uint16_t* H, int32_t M, int32_t d, int64_t ldh,
+                         const uint16_t* W_high, int32_t V_high,
+                         const int32_t* t2f, const float* bias_high,
+                         double temperature, int32_t mode, uint64_t seed,
+                         uint64_t offset, int32_t k, int32_t* ids,
+                         double* probs, double* scores, double* top_logits,
+                         int32_t* trimmed_idx, double* row_max,
+                         double* row_sumexp) {
+  if (M < 0 || d <= 0 || V_high <= 0 || k <= 0 || k > V_high) return 1;
+  if (!(temperature > 0.0) || (mode != 0 && mode != 1)) return 1;
+  std::vector<double> logits(static_cast<size_t>(V_high));
+  std::vector<double> s(static_cast<size_t>(V_high));
+  std::vector<double> key(static_cast<size_t>(V_high));
+  std::vector<int32_t> order(static_cast<size_t>(V_high));
+  auto full_id = [&](int32_t i) { return t2f ? t2f[i] : i; };
+  for (int32_t m = 0; m < M; ++m) {
+    oracle_head_logits(H + static_cast<int64_t>(m) * ldh, 1, d, ldh, W_high,
+                       V_high, logits.data());
+    for (int32_t i = 0; i < V_high; ++i) {
+      logits[i] += bias_high ? static_cast<double>(bias_high[i]) : 0.0;
+      s[i] = logits[i] / temperature;
+    }
+    double mx = s[0];
+    for (int32_t i = 1; i < V_high; ++i) mx = std::max(mx, s[i]);
+    double sumexp = 0.0;
+    for (int32_t i = 0; i < V_high; ++i) sumexp += std::exp(s[i] - mx);
+    for (int32_t i = 0; i < V_high; ++i)
+      key[i] = s[i] + (mode == 1 ? gumbel_noise(seed, offset, m, full_id(i)) : 0.0);
+
+    for (int32_t i = 0; i < V_high; ++i) order[i] = i;
+    std::partial_sort(order.begin(), order.begin() + k, order.end(),
+                      [&](int32_t a, int32_t b) {
+                        if (key[a] != key[b]) return key[a] > key[b];
+                        return full_id(a) < full_id(b);
+                      });
+    for (int32_t r = 0; r < k; ++r) {
+      const int32_t i = order[r];
+      const int64_t o = static_cast<int64_t>(m) * k + r;
+      if (ids) ids[o] = full_id(i);
+      if (probs) probs[o] = std::exp(s[i] - mx) / sumexp;
+      if (scores) scores[o] = key[i];
       if (top_logits) top_logits[o] = logits[i];
       if (trimmed_idx) trimmed_idx[o] = i;
     }

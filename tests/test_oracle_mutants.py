@@ -36,10 +36,39 @@ MUTANTS = {
                          "std::exp(logits[i] - mx) / (sumexp + 1e-9);"),
 }
 
+# Mistakes in the head's options (bias, temperature, sampling); these are
+# run against the options pins.
+OPTION_MUTANTS = {
+    "gumbel_sign": ("return -std::log(-std::log(u));",
+                    "return std::log(-std::log(u));"),
+    "exponential_not_gumbel": ("return -std::log(-std::log(u));",
+                               "return -std::log(u);"),
+    "uniform_wrong_scale": ("+ 0.5) / 8388608.0;", "+ 0.5) / 16777216.0;"),
+    "temperature_multiplies": ("s[i] = logits[i] / temperature;",
+                               "s[i] = logits[i] * temperature;"),
+    "bias_dropped": ("logits[i] += bias_high ? static_cast<double>(bias_high[i]) : 0.0;",
+                     "logits[i] += 0.0;"),
+    "philox_no_key_bump": ("k[0] += kWeyl0;", "k[0] += 0u;"),
+    "philox_swapped_halves": ("c[1] = lo1;", "c[1] = lo0;"),
+    "noise_by_trimmed_index": ("gumbel_noise(seed, offset, m, full_id(i))",
+                               "gumbel_noise(seed, offset, m, i)"),
+    "noise_ignores_row": ("static_cast<uint32_t>(full_id), static_cast<uint32_t>(m),",
+                          "static_cast<uint32_t>(full_id), 0u,"),
+    "noise_ignores_offset_high": ("static_cast<uint32_t>(offset >> 32)};",
+                                  "0u};"),
+    "sample_prob_of_score": ("if (probs) probs[o] = std::exp(s[i] - mx) / sumexp;\n      if (scores)",
+                             "if (probs) probs[o] = std::exp(key[i] - mx) / sumexp;\n      if (scores)"),
+}
 
-@pytest.mark.parametrize("name", sorted(MUTANTS))
+
+ALL = {**{n: (m, "test_oracle_pins.py") for n, m in MUTANTS.items()},
+       **{n: (m, "test_oracle_pins_options.py")
+          for n, m in OPTION_MUTANTS.items()}}
+
+
+@pytest.mark.parametrize("name", sorted(ALL))
 def test_pins_catch_mutant(name, tmp_path):
-    old, new = MUTANTS[name]
+    (old, new), pins = ALL[name]
     src = open(SRC).read()
     assert src.count(old) >= 1, f"mutation anchor for {name} not found"
     mutated = src.replace(old, new)
@@ -51,7 +80,7 @@ def test_pins_catch_mutant(name, tmp_path):
     env = dict(os.environ, FRD_ORACLE_LIB=str(lib))
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p",
                         "no:cacheprovider",
-                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                        os.path.join(ROOT, "tests", pins)],
                        env=env, cwd=ROOT, capture_output=True, text=True,
                        timeout=600)
     assert r.returncode != 0, f"no pin caught mutant {name}:\n{r.stdout[-2000:]}"
