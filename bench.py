@@ -413,6 +413,21 @@ def run_ours(args, world, rank, local):
     full_per_call = max_over_ranks(full_secs, world) / full_steps
     full_bytes = V * d * 2 + M * d * 2 + M * k * 8
 
+    # ---- the same draft step drawing its token (Gumbel-max, T = 1)
+    ids1 = torch.empty(M, 1, dtype=torch.int32, device=dev)
+    probs1 = torch.empty(M, 1, dtype=torch.float32, device=dev)
+
+    def sample_step(i):
+        vt.draft_head(H, W_highs[i % n_copies], t2f, 1, out_ids=ids1,
+                      out_probs=probs1, ws=ws, sample=True, seed=1234,
+                      offset=i)
+
+    sample_steps = min(args.steps, 5000)
+    sample_secs, _ = time_graph(torch, sample_step, sample_steps,
+                                max(3, args.warmup // 4))
+    sample_per_call = max_over_ranks(sample_secs, world) / sample_steps
+    sample_bytes = V_high * d * 2 + M * d * 2 + M * 8
+
     out = {
         "metric": METRIC, "value": value, "unit": "calls/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -434,13 +449,21 @@ def run_ours(args, world, rank, local):
                      "peak_kind": peak_kind,
                      "traffic": committed_traffic(),
                      "alg_bytes_per_launch": alg_bytes,
-                     "kernel": "head_gemv_kernel<1,16,1>"},
+                     "kernel": "head_gemv_kernel<1,16,1,false>"},
         "e2e": {"value": e2e_value, "unit": "calls/s",
                 "h2d_bytes_per_step": M * d * 2,
                 "d2h_bytes_per_step": M * k * 8,
                 "steps": e2e_steps},
         "gpu_launches": args.steps,
         "clocks": clocks,
+        "sample": {
+            "mode": "one Gumbel-max draw per call (Philox4x32-10 noise), "
+                    "temperature 1, same workload",
+            "us_per_call": sample_per_call * 1e6,
+            "calls_per_s": 1.0 / sample_per_call,
+            "achieved_gbs": sample_bytes / sample_per_call / 1e9,
+            "frac": sample_bytes / sample_per_call / 1e9 / peak,
+        },
         "full_vocab": {
             "V": V, "us_per_call": full_per_call * 1e6,
             "calls_per_s": 1.0 / full_per_call,

@@ -41,6 +41,15 @@ class VTError(RuntimeError):
 _lib = None
 _lock = threading.Lock()
 
+VT_HEAD_TOPK, VT_HEAD_SAMPLE = 0, 1
+
+
+class HeadOptions(ctypes.Structure):
+    """``vt_head_options`` of the C ABI."""
+    _fields_ = [("bias_high", ctypes.c_void_p), ("temperature", ctypes.c_float),
+                ("mode", ctypes.c_int32), ("seed", ctypes.c_uint64),
+                ("offset", ctypes.c_uint64)]
+
 
 def library_path() -> str:
     return _build.LIB_PATH
@@ -69,9 +78,15 @@ def load(build_if_missing: bool = True):
             "vt_select_vocab_workspace_size": ([i32], sz),
             "vt_select_vocab": ([p, i32, i32, p, p, p, p, sz, p], ctypes.c_int),
             "vt_gather_rows": ([p, i64, i32, p, i32, p, p, p], ctypes.c_int),
+            "vt_gather_bias": ([p, i64, p, i32, p, p, p], ctypes.c_int),
             "vt_draft_head_workspace_size": ([i32, i32, i32], sz),
             "vt_draft_head": ([p, i32, i32, i64, p, i32, p, i32, p, p, p, p,
                                sz, p], ctypes.c_int),
+            "vt_draft_head_ex": ([p, i32, i32, i64, p, i32, p, i32,
+                                  ctypes.POINTER(HeadOptions), p, p, p, p, sz,
+                                  p], ctypes.c_int),
+            "vt_draft_noise": ([ctypes.c_uint64, ctypes.c_uint64, i32, p, i64,
+                                p, p], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -217,9 +232,17 @@ def draft_head(H: torch.Tensor, W_high: torch.Tensor, t2f: torch.Tensor | None,
                k: int, out_ids: torch.Tensor | None = None,
                out_probs: torch.Tensor | None = None,
                out_logits: torch.Tensor | None = None,
-               ws: torch.Tensor | None = None):
+               ws: torch.Tensor | None = None, *,
+               bias: torch.Tensor | None = None, temperature: float = 1.0,
+               sample: bool = False, seed: int = 0, offset: int = 0):
     """One draft step: top-k full-vocabulary ids and softmax probabilities
-    over the V_high kept rows for each of the M hidden states in ``H``."""
+    over the V_high kept rows for each of the M hidden states in ``H``.
+
+    With options (vt_draft_head_ex): ``bias`` (fp32 [V_high]) is added to
+    every logit, probabilities are softmax(logit / temperature), and
+    ``sample=True`` draws instead of taking the top-k (k = 1: one draw;
+    k > 1: draws without replacement), with the generator keyed by
+    ``seed`` and the step counter ``offset``."""
     _cuda(W_high, "W_high", torch.bfloat16)
     if not (isinstance(H, torch.Tensor) and H.is_cuda and H.dtype == torch.bfloat16
             and H.dim() == 2 and H.stride(1) == 1):
@@ -241,11 +264,59 @@ def draft_head(H: torch.Tensor, W_high: torch.Tensor, t2f: torch.Tensor | None,
     nbytes = lib.vt_draft_head_workspace_size(M, V_high, k)
     if ws is None:
         ws = _ws.get("head", nbytes, dev, zeroed=True)
-    _check("vt_draft_head", lib.vt_draft_head(
+    if bias is None and temperature == 1.0 and not sample:
+        _check("vt_draft_head", lib.vt_draft_head(
+            _ptr(H), M, d, H.stride(0), _ptr(W_high), V_high, _ptr(t2f), k,
+            _ptr(out_ids), _ptr(out_probs), _ptr(out_logits), _ptr(ws),
+            ws.numel(), _stream(dev)))
+        return out_ids, out_probs
+    if bias is not None:
+        _cuda(bias, "bias", torch.float32)
+        if bias.numel() != V_high:
+            raise ValueError("bias must hold V_high values")
+    opts = HeadOptions(_ptr(bias), float(temperature),
+                       VT_HEAD_SAMPLE if sample else VT_HEAD_TOPK,
+                       int(seed) & (2**64 - 1), int(offset) & (2**64 - 1))
+    _check("vt_draft_head_ex", lib.vt_draft_head_ex(
         _ptr(H), M, d, H.stride(0), _ptr(W_high), V_high, _ptr(t2f), k,
-        _ptr(out_ids), _ptr(out_probs), _ptr(out_logits), _ptr(ws), ws.numel(),
-        _stream(dev)))
+        ctypes.byref(opts), _ptr(out_ids), _ptr(out_probs), _ptr(out_logits),
+        _ptr(ws), ws.numel(), _stream(dev)))
     return out_ids, out_probs
+
+
+def gather_bias(b: torch.Tensor, t2f: torch.Tensor,
+                out: torch.Tensor | None = None,
+                n_invalid: torch.Tensor | None = None) -> torch.Tensor:
+    """b_high = b[t2f]: the kept rows' bias (fp32), for ``bias=`` of
+    draft_head."""
+    _cuda(b, "b", torch.float32)
+    _cuda(t2f, "t2f", torch.int32)
+    dev = b.device
+    if out is None:
+        out = torch.empty(t2f.numel(), dtype=torch.float32, device=dev)
+    _cuda(out, "out", torch.float32)
+    if n_invalid is not None:
+        _cuda(n_invalid, "n_invalid", torch.int64)
+    _check("vt_gather_bias", load().vt_gather_bias(
+        _ptr(b), b.numel(), _ptr(t2f), t2f.numel(), _ptr(out), _ptr(n_invalid),
+        _stream(dev)))
+    return out
+
+
+def draft_noise(seed: int, offset: int, m: int, full_ids: torch.Tensor,
+                out: torch.Tensor | None = None) -> torch.Tensor:
+    """The Gumbel noise the sampling head adds to each of ``full_ids``
+    (int32, device) for hidden state m at (seed, offset)."""
+    _cuda(full_ids, "full_ids", torch.int32)
+    dev = full_ids.device
+    if out is None:
+        out = torch.empty(full_ids.numel(), dtype=torch.float32, device=dev)
+    _cuda(out, "out", torch.float32)
+    lib = load()
+    _check("vt_draft_noise", lib.vt_draft_noise(
+        int(seed) & (2**64 - 1), int(offset) & (2**64 - 1), m, _ptr(full_ids),
+        full_ids.numel(), _ptr(out), _stream(dev)))
+    return out
 
 
 def draft_head_host(H_host: torch.Tensor, W_high: torch.Tensor,
@@ -271,12 +342,15 @@ def draft_head_host(H_host: torch.Tensor, W_high: torch.Tensor,
 
 
 def build_vocab(tokens: torch.Tensor, V: int, V_high: int,
-                W: torch.Tensor | None = None):
+                W: torch.Tensor | None = None, b: torch.Tensor | None = None):
     """The offline build in one call: histogram, selection, maps and (if
-    ``W`` is given) the gathered W_high.  Returns a dict of device tensors."""
+    ``W`` / ``b`` are given) the gathered W_high / b_high.  Returns a dict of
+    device tensors."""
     counts, n_invalid = count_tokens(tokens, V)
     t2f, f2t, sums = select_vocab(counts, V_high)
     out = dict(counts=counts, n_invalid=n_invalid, t2f=t2f, f2t=f2t, sums=sums)
     if W is not None:
         out["W_high"] = gather_rows(W, t2f)
+    if b is not None:
+        out["b_high"] = gather_bias(b, t2f)
     return out

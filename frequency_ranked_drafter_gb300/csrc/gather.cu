@@ -1,8 +1,9 @@
-// vt_gather_rows — reconstruction of the trimmed lm_head.
+// vt_gather_rows / vt_gather_bias — reconstruction of the trimmed lm_head.
 //
 // "VocabTrim: Memory-Efficient Vocabulary Pruning for Speculative Decoding",
 // Implementation Step 3: the trimmed weight is the original [vocab, hidden]
-// weight indexed by trimmed_to_full along its rows.
+// weight indexed by trimmed_to_full along its rows, and an existing bias is
+// indexed the same way.
 //
 // HBM-bound copy: every kept row (d bf16 = 2d bytes) is read once and written
 // once.  One warp moves one row at a time with 16-byte loads; each lane keeps
@@ -50,8 +51,45 @@ __global__ void __launch_bounds__(kGatherThreads, 4)
   }
 }
 
+// b_high[i] = b[t2f[i]]: one thread per kept id (a 1-D gather of 4-byte
+// values, V_high * 8 bytes of traffic; launch latency dominates).
+__global__ void gather_bias_kernel(const float* __restrict__ b, int64_t V,
+                                   const int32_t* __restrict__ t2f, int V_high,
+                                   float* __restrict__ b_high,
+                                   unsigned long long* __restrict__ n_invalid) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < V_high;
+       i += gridDim.x * blockDim.x) {
+    const int64_t src = t2f[i];
+    const bool ok = src >= 0 && src < V;
+    b_high[i] = ok ? b[src] : 0.0f;
+    if (!ok && n_invalid) atomicAdd(n_invalid, 1ull);
+  }
+}
+
 }  // namespace
 }  // namespace vt
+
+extern "C" vt_status vt_gather_bias(const float* b, int64_t V,
+                                    const int32_t* t2f, int32_t V_high,
+                                    float* b_high, uint64_t* n_invalid,
+                                    void* stream) {
+  using namespace vt;
+  if (!b || !t2f || !b_high)
+    return fail(VT_ERR_INVALID_ARG, "vt_gather_bias: null pointer");
+  if (V <= 0 || V_high <= 0)
+    return fail(VT_ERR_INVALID_ARG, "vt_gather_bias: need V > 0, V_high > 0");
+  if (!aligned(b, 4) || !aligned(b_high, 4))
+    return fail(VT_ERR_INVALID_ARG, "vt_gather_bias: b, b_high not 4B aligned");
+  if (b < b_high + V_high && b_high < b + V)
+    return fail(VT_ERR_INVALID_ARG, "vt_gather_bias: b_high overlaps b");
+  DeviceInfo di;
+  if (!current_device(&di)) return VT_ERR_CUDA;
+  const int grid = (int)std::min<int64_t>(((int64_t)V_high + 255) / 256,
+                                          (int64_t)di.num_sms * 4);
+  gather_bias_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(
+      b, V, t2f, V_high, b_high, reinterpret_cast<unsigned long long*>(n_invalid));
+  return launch_status("gather_bias_kernel");
+}
 
 extern "C" vt_status vt_gather_rows(const uint16_t* W, int64_t V, int32_t d,
                                     const int32_t* t2f, int32_t V_high,

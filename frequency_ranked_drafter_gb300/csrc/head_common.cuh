@@ -21,12 +21,25 @@ constexpr int kHeadTicketBytes = 2048;
 constexpr int kHeadRowTicketOffset = 1024;
 constexpr int kStageBytesMax = 96 * 1024;  // staged candidates, last CTA
 
+// Options of a head call (vt_head_options): kept-row bias added to every
+// logit, temperature T (probabilities are softmax(logit / T); the kernels
+// multiply by the fp32 reciprocal of T, exact for T = 1), and the
+// selection: the k largest logit / T, or (sample) the k largest
+// logit / T + g with g the Gumbel noise of the token (gumbel_noise).
+struct HeadOpts {
+  const float* bias;  // [V_high] or null
+  float tau;
+  int sample;
+  uint64_t seed, offset;
+};
+
 // Each CTA b publishes, per hidden state m, one record of `pstride` 32-bit
 // words at part + (m * G + b) * pstride (G CTAs), 16-byte aligned so that
 // the records of one m are a single bulk copy:
-//   [0] max logit of its rows, [1] sum of exp(logit - max) over its rows,
-//   [2, 4) unused, [4, 4+2k) its k best entries as 64-bit keys of (logit,
-//   full-vocabulary id) (make_key), best first; unused slots kEmptyKey.
+//   [0] max of logit/T over its rows, [1] sum of exp(logit/T - max),
+//   [2, 4) unused, [4, 4+2k) its k best entries as 64-bit keys of
+//   (selection score, full-vocabulary id) (make_key), best first, unused
+//   slots kEmptyKey; sampling only: [4+2k, 4+3k) the entries' logit/T.
 struct HeadArgs {
   const uint16_t* H;
   int64_t ldh;
@@ -43,15 +56,58 @@ struct HeadArgs {
   int pstride;
   unsigned* ticket;      // [0]: CTAs done; [1]: next dynamically dealt row group
   unsigned* err;         // device error word (VT_ERR_TIMEOUT if a wait gave up)
+  HeadOpts opt;
+  int m_base;            // index of this launch's first hidden state in the call
 };
 
-inline int head_pstride(int k) { return (4 + 2 * k + 3) / 4 * 4; }
+inline int head_pstride(int k, bool sample) {
+  return (4 + (sample ? 3 : 2) * k + 3) / 4 * 4;
+}
 
 // Workspace of one GEMV launch over MR hidden states: the shared header and
 // up to kHeadMaxCtas CTAs' partials.
-inline size_t head_gemv_workspace(int MR, int k) {
+inline size_t head_gemv_workspace(int MR, int k, bool sample) {
   return (size_t)kHeadTicketBytes +
-         (size_t)kHeadMaxCtas * MR * head_pstride(k) * sizeof(float);
+         (size_t)kHeadMaxCtas * MR * head_pstride(k, sample) * sizeof(float);
+}
+
+// Philox4x32-10, the counter-based generator of Salmon, Moraes, Dror and
+// Shaw ("Parallel Random Numbers: As Easy as 1, 2, 3", SC 2011): ten rounds,
+// each multiplying counter words 0 and 2 by the round multipliers (high and
+// low halves of the 64-bit products) and mixing in the key, which advances by
+// the Weyl increments between rounds.  Returns output word 0.
+__device__ __forceinline__ uint32_t philox4x32_10_w0(uint32_t c0, uint32_t c1,
+                                                     uint32_t c2, uint32_t c3,
+                                                     uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int round = 0; round < 10; ++round) {
+    if (round > 0) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    const uint32_t lo0 = 0xD2511F53u * c0, hi0 = __umulhi(0xD2511F53u, c0);
+    const uint32_t lo1 = 0xCD9E8D57u * c2, hi1 = __umulhi(0xCD9E8D57u, c2);
+    const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+    c0 = n0;
+    c1 = lo1;
+    c2 = n2;
+    c3 = lo0;
+  }
+  return c0;
+}
+
+// Gumbel noise of token `full_id` for hidden state m at step (seed, offset):
+// x = word 0 of Philox4x32-10 at counter (full_id, m, offset low, offset
+// high), key (seed low, seed high); u = ((x >> 9) + 1/2) / 2^23 in (0, 1),
+// exact in binary32; g = -log(-log(u)).  Keyed by the full-vocabulary id, so
+// a token's noise does not depend on which tokens were kept or where.
+__device__ __forceinline__ float gumbel_noise(uint64_t seed, uint64_t offset,
+                                              int m, int full_id) {
+  const uint32_t x = philox4x32_10_w0((uint32_t)full_id, (uint32_t)m,
+                                      (uint32_t)offset, (uint32_t)(offset >> 32),
+                                      (uint32_t)seed, (uint32_t)(seed >> 32));
+  const float u = ((float)(x >> 9) + 0.5f) * 0x1p-23f;
+  return -logf(-logf(u));
 }
 
 // Arrival on a grid-wide ticket: atomic increment with acquire-release
@@ -190,6 +246,7 @@ __device__ __forceinline__ void cta_merge_lists(entry_key& x, int& y, ListSlots&
 struct MergeScratch {
   ListSlots slots;
   entry_key surv[kTopKMax * kTopKMax];  // entries reaching the k-th head
+  float surv_s[kTopKMax * kTopKMax];    // ... their logit/T (sampling)
   int q_list[kTopKMax];                 // the lists with the k best heads
   float w_max[kMergeMaxWarps];
   float w_sum[kMergeMaxWarps];
@@ -342,7 +399,12 @@ __device__ void head_final_merge(const HeadArgs& a, int MR, int G, float* stage,
       const int b = sc.q_list[j];
       if (b < 0) continue;
       const entry_key x = list(b)[c - j * k];
-      if (x >= t && x != kEmptyKey) sc.surv[atomicAdd(&sc.cnt, 1)] = x;
+      if (x >= t && x != kEmptyKey) {
+        const int p = atomicAdd(&sc.cnt, 1);
+        sc.surv[p] = x;
+        if (a.opt.sample)
+          sc.surv_s[p] = reinterpret_cast<const float*>(list(b) + k)[c - j * k];
+      }
     }
     float mg = sc.w_max[0];
 #pragma unroll
@@ -361,13 +423,16 @@ __device__ void head_final_merge(const HeadArgs& a, int MR, int G, float* stage,
     const int S = sc.cnt;
     int32_t* ids = a.out_ids + (size_t)m * k;
     float* probs = a.out_probs + (size_t)m * k;
+    // (sampling: the key is the score; the logit/T of list entries follows
+    // the keys in the record)
     for (int c = tid; c < S; c += NT) {
       const entry_key x = sc.surv[c];
       int rank = 0;
       for (int q = 0; q < S; ++q) rank += sc.surv[q] > x;
       if (rank < k) {
         ids[rank] = key_id(x);
-        probs[rank] = expf(key_logit(x) - mg) / sg;
+        const float sv = a.opt.sample ? sc.surv_s[c] : key_logit(x);
+        probs[rank] = expf(sv - mg) / sg;
       }
     }
     __syncthreads();
@@ -384,7 +449,8 @@ constexpr int kHeadTcMinM = 2;
 size_t head_tc_workspace(int M, int V_high, int k);
 vt_status head_tc(const uint16_t* H, int M, int d, int64_t ldh,
                   const uint16_t* W, int V_high, const int32_t* t2f, int k,
-                  int32_t* out_ids, float* out_probs, float* out_logits,
-                  void* ws, const DeviceInfo& di, cudaStream_t s);
+                  const HeadOpts& opt, int32_t* out_ids, float* out_probs,
+                  float* out_logits, void* ws, const DeviceInfo& di,
+                  cudaStream_t s);
 
 }  // namespace vt

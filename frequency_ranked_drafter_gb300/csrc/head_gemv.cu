@@ -16,10 +16,14 @@
 //     round-robin over all warps of the grid and the last eighth one group
 //     at a time from a counter, so every SM streams about the same bytes
 //     and all finish together;
-//   * each warp keeps, per hidden state, an online (max, sum of exp) and a
-//     sorted top-k list held one entry per lane (insertion by ballot and a
-//     one-lane shift), so no logit is ever written to memory;
-//   * each CTA merges its warps' lists by rank counting in shared memory and
+//   * each warp keeps, per hidden state, an online (max, sum of exp) of
+//     s = (logit + bias) / T and a sorted list of its k best entries, one
+//     64-bit key of (score, full id) per lane (insertion by ballot and a
+//     one-lane shift), so no logit is ever written to memory; the score is s
+//     for top-k and s + Gumbel noise of the token when sampling ("VocabTrim",
+//     Step 4 draws from the trimmed softmax; the Gumbel-max rule draws from
+//     the same distribution);
+//   * each CTA merges its warps' lists in registers (cta_merge_lists) and
 //     publishes (max, sumexp, top-k) to the workspace; the last CTA to finish
 //     (atomic ticket, no waiting) merges all CTAs (head_final_merge),
 //     rescales the sums, writes ids and probabilities and re-arms the ticket.
@@ -52,7 +56,7 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-template <int MR, int CPL, int U>
+template <int MR, int CPL, int U, bool kSample>
 __global__ void __launch_bounds__(kGemvThreads, 2)
     head_gemv_kernel(HeadArgs a) {
   extern __shared__ __align__(16) float hs[];  // [MR][d] fp32 hidden states
@@ -76,15 +80,19 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
   }
   __syncthreads();
 
-  // Per hidden state: running max and sum of exp (online softmax), and the
-  // warp's k best entries as keys of (logit, full-vocabulary id), lane j
-  // holding the j-th best, with thr the k-th.
-  float mx[MR], se[MR];
+  // Per hidden state: running max and sum of exp of s = logit / T (online
+  // softmax), and the warp's k best entries as keys of (score, full id),
+  // lane j holding the j-th best, with thr the k-th.  The score is s, or
+  // s + Gumbel noise when sampling; then ts carries each entry's s.
+  float mx[MR], se[MR], ts[MR];
   entry_key tk[MR], thr[MR];
 #pragma unroll
   for (int m = 0; m < MR; ++m) {
-    mx[m] = -INFINITY; se[m] = 0.f; tk[m] = kEmptyKey; thr[m] = kEmptyKey;
+    mx[m] = -INFINITY; se[m] = 0.f; ts[m] = -INFINITY;
+    tk[m] = kEmptyKey; thr[m] = kEmptyKey;
   }
+  const float* bias = a.opt.bias;
+  const float inv_tau = 1.0f / a.opt.tau;
 
   const int nchunks = d >> 3;
   const int nkb = (nchunks + 32 * CPL - 1) / (32 * CPL);
@@ -95,13 +103,17 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
 
   auto process_group = [&](int g) {
     const int r0 = g * U;
-    // full ids of the group's rows, fetched while the rows stream in
+    // full ids (and biases) of the group's rows, fetched while the rows
+    // stream in
     int fid[U];
+    float brow[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int row = min(r0 + u, a.V_high - 1);
       fid[u] = a.t2f ? __ldg(a.t2f + row) : row;
+      brow[u] = bias ? __ldg(bias + row) : 0.f;
     }
+    float noise[U][MR];
     float acc[U][MR];
 #pragma unroll
     for (int u = 0; u < U; ++u)
@@ -120,6 +132,13 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
           const int c = kb * 32 * CPL + lane + 32 * j;
           wv[u][j] = c < nchunks ? ld_stream_u4(wrow + c) : make_uint4(0, 0, 0, 0);
         }
+      }
+      if (kSample && kb == 0) {  // generator work overlaps the row loads
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+          for (int m = 0; m < MR; ++m)
+            noise[u][m] = gumbel_noise(a.opt.seed, a.opt.offset, a.m_base + m, fid[u]);
       }
 #pragma unroll
       for (int j = 0; j < CPL; ++j) {
@@ -142,21 +161,28 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
       if (row >= a.V_high) break;
 #pragma unroll
       for (int m = 0; m < MR; ++m) {
-        const float l = warp_sum(acc[u][m]);
+        const float l = warp_sum(acc[u][m]) + brow[u];
         if (a.out_logits && lane == 0)
           a.out_logits[(int64_t)m * a.V_high + row] = l;
-        if (l > mx[m]) {
-          se[m] = se[m] * __expf(mx[m] - l) + 1.f;
-          mx[m] = l;
+        const float sv = l * inv_tau;  // exact for T = 1
+        if (sv > mx[m]) {
+          se[m] = se[m] * __expf(mx[m] - sv) + 1.f;
+          mx[m] = sv;
         } else {
-          se[m] += __expf(l - mx[m]);
+          se[m] += __expf(sv - mx[m]);
         }
-        const entry_key key = make_key(l, fid[u]);
+        const entry_key key = make_key(kSample ? sv + noise[u][m] : sv, fid[u]);
         if (key > thr[m]) {  // insert at its rank, the k-th drops out
           const int p = __popc(__ballot_sync(~0u, lane < k && tk[m] > key));
           const entry_key up = __shfl_up_sync(~0u, tk[m], 1);
-          if (lane == p) tk[m] = key;
-          else if (lane > p && lane < k) tk[m] = up;
+          const float ups = kSample ? __shfl_up_sync(~0u, ts[m], 1) : 0.f;
+          if (lane == p) {
+            tk[m] = key;
+            ts[m] = sv;
+          } else if (lane > p && lane < k) {
+            tk[m] = up;
+            ts[m] = ups;
+          }
           thr[m] = __shfl_sync(~0u, tk[m], k - 1);
         }
       }
@@ -195,10 +221,13 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
 #pragma unroll
   for (int m = 0; m < MR; ++m) {
     entry_key x = tk[m];
-    int unused = 0;
-    cta_merge_lists<kGemvWarps, false>(x, unused, msc.slots, level);
+    int y = __float_as_int(ts[m]);
+    cta_merge_lists<kGemvWarps, kSample>(x, y, msc.slots, level);
     if (warp == 0) {
-      if (lane < k) reinterpret_cast<entry_key*>(rec[m] + 4)[lane] = x;
+      if (lane < k) {
+        reinterpret_cast<entry_key*>(rec[m] + 4)[lane] = x;
+        if (kSample) rec[m][4 + 2 * k + lane] = __int_as_float(y);
+      }
       const float wmx = lane < kGemvWarps ? w_mx[m][lane] : -INFINITY;
       const float wse = lane < kGemvWarps ? w_se[m][lane] : 0.f;
       float M_b = wmx;
@@ -226,10 +255,10 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
   }
 }
 
-template <int MR, int CPL, int U>
+template <int MR, int CPL, int U, bool kSample>
 vt_status launch_gemv(const HeadArgs& a, const DeviceInfo& di,
                       cudaStream_t s) {
-  auto kern = head_gemv_kernel<MR, CPL, U>;
+  auto kern = head_gemv_kernel<MR, CPL, U, kSample>;
   const int64_t groups = (a.V_high + U - 1) / U;
   // Two CTAs of 8 warps per SM (the launch bound); no more CTAs than warps
   // have rows, and no more than the last CTA can stage records of.
@@ -252,7 +281,8 @@ template <int MR, int CPL>
 vt_status launch_cpl(const HeadArgs& a, const DeviceInfo& di, cudaStream_t s) {
   constexpr int U0 = 16 / CPL < 8 / MR ? 16 / CPL : 8 / MR;
   constexpr int U = U0 < 1 ? 1 : U0;
-  return launch_gemv<MR, CPL, U>(a, di, s);
+  return a.opt.sample ? launch_gemv<MR, CPL, U, true>(a, di, s)
+                      : launch_gemv<MR, CPL, U, false>(a, di, s);
 }
 
 template <int MR>

@@ -94,7 +94,7 @@ extern "C" vt_status vt_draft_head_noalloc(const uint16_t* H, int32_t M,
                 "vt_draft_head_noalloc: H, W_high not 16B aligned");
   // Hidden states are processed four at a time by the GEMV kernel, each
   // group reusing the same scratch, so the need depends on min(M, 4) and k.
-  const size_t need = head_gemv_workspace(std::min(M, 4), k);
+  const size_t need = head_gemv_workspace(std::min(M, 4), k, /*sample=*/false);
   if (need > kNoAllocScratchBytes)
     return fail(VT_ERR_UNSUPPORTED,
                 "vt_draft_head_noalloc: needs " + std::to_string(need) +
@@ -114,13 +114,15 @@ extern "C" vt_status vt_draft_head_noalloc(const uint16_t* H, int32_t M,
   a.V_high = V_high;
   a.t2f = t2f;
   a.k = k;
-  a.pstride = head_pstride(k);
+  a.pstride = head_pstride(k, false);
+  a.opt = HeadOpts{nullptr, 1.0f, 0, 0, 0};
   a.ticket = static_cast<unsigned*>(scratch);
   a.err = reinterpret_cast<unsigned*>(static_cast<char*>(scratch) + 128);
   a.part = reinterpret_cast<float*>(static_cast<char*>(scratch) +
                                     kHeadTicketBytes);
   for (int m0 = 0; m0 < M; m0 += 4) {
     a.M = std::min(4, M - m0);
+    a.m_base = m0;
     a.H = H + (int64_t)m0 * ldh;
     a.out_ids = out_ids + (int64_t)m0 * k;
     a.out_probs = out_probs + (int64_t)m0 * k;

@@ -19,11 +19,13 @@
 // fp32 logits (tile rows along lanes, so every store is a coalesced 128-byte
 // row segment).  At these M the work stays bound by the W_high stream.
 //
-// Softmax + top-k: each hidden state's V_high logits (L2-resident) are
-// split over CTAs of 4096; each CTA reduces its part to (max, sum of exp,
-// exact top-k) and the last CTA of the row merges the parts.  Entries carry
-// their full-vocabulary id (t2f read next to the logits), which breaks ties
-// between equal logits (lower id first) and is what the call returns.
+// Softmax + top-k: each hidden state's V_high logits (L2-resident, bias
+// added by the GEMM epilogue) are split over CTAs of 4096; each CTA reduces
+// its part to (max, sum of exp of logit/T, exact top-k of the selection
+// score) and the last CTA of the row merges the parts.  The score is
+// logit/T, or logit/T plus the token's Gumbel noise when sampling.  Entries
+// carry their full-vocabulary id (t2f read next to the logits), which breaks
+// ties between equal scores (lower id first) and is what the call returns.
 //
 // Every wait on an mbarrier is bounded (kWaitBudget cycles, about a
 // second); a wait that gives up records VT_ERR_TIMEOUT in the error word of
@@ -51,6 +53,7 @@ struct TcArgs {
   int stages;
   uint32_t tmem_cols;
   float* logits;  // [M][V_high]
+  const float* bias;  // [V_high] or null, added to every logit
   unsigned* err;
 };
 
@@ -195,9 +198,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                           r);
         tc::tmem_ld_wait();
         if (row < a.V_high) {
+          const float b = a.bias ? __ldg(a.bias + row) : 0.f;
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            if (c0 + j < a.M) a.logits[(size_t)(c0 + j) * a.V_high + row] = r[j];
+            if (c0 + j < a.M) a.logits[(size_t)(c0 + j) * a.V_high + row] = r[j] + b;
         }
       }
       tc::tc_fence_before();
@@ -230,14 +234,23 @@ constexpr int kRowSpan = kRowThreads * kRowVals;  // 4096 logits per CTA
 constexpr int kRowSurvivors = 2048;
 
 struct RowArgs {
-  const float* logits;  // [M][V_high]
+  const float* logits;  // [M][V_high], bias already added
   int V_high, k, P;
   const int32_t* t2f;
   int32_t* out_ids;
   float* out_probs;
   unsigned* tickets;  // [M], zero between calls
-  float* part;        // [M][P][2 + 2k]
+  float* part;        // [M][P][2 + 3k]
+  float inv_tau;  // 1 / T
+  int sample;
+  uint64_t seed, offset;
 };
+
+// Selection score of one logit: s = logit / T, plus the token's Gumbel noise
+// when sampling.
+__device__ __forceinline__ float row_score(const RowArgs& a, int m, float s, int f) {
+  return a.sample ? s + gumbel_noise(a.seed, a.offset, m, f) : s;
+}
 
 __global__ void __launch_bounds__(kRowThreads)
     rows_topk_kernel(RowArgs a) {
@@ -245,18 +258,20 @@ __global__ void __launch_bounds__(kRowThreads)
   __shared__ float red[kWarps];
   __shared__ float tw_v[kWarps];
   __shared__ int tw_i[kWarps];
-  __shared__ float2 surv[kRowSurvivors];
+  __shared__ float2 surv[kRowSurvivors];  // (score, full id)
+  __shared__ float surv_s[kRowSurvivors]; // logit / T of the survivor
   __shared__ int s_cnt, s_last;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int m = blockIdx.y, part_idx = blockIdx.x, k = a.k;
-  const int ps = 2 + 2 * k;
+  const int ps = 2 + 3 * k;
   const float* row = a.logits + (size_t)m * a.V_high;
   const int base = part_idx * kRowSpan;
 
   // this thread's values: 4 float4 at base + 4*(tid + 256*q) (or scalars
-  // when the row is not 16-byte aligned or at the tail), and their
-  // full-vocabulary ids, which break ties between equal logits
-  float v[kRowVals];
+  // when the row is not 16-byte aligned or at the tail) as s = logit / T,
+  // their full-vocabulary ids (which break ties between equal scores) and
+  // their selection scores
+  float v[kRowVals], sc[kRowVals];
   int f[kRowVals];
   const bool vec = ((a.V_high & 3) == 0) &&
                    ((reinterpret_cast<uintptr_t>(a.logits) & 15) == 0);
@@ -283,8 +298,11 @@ __global__ void __launch_bounds__(kRowThreads)
   int bi = INT_MAX;
 #pragma unroll
   for (int j = 0; j < kRowVals; ++j) {
+    const bool in = idx_of(j) < a.V_high;
+    v[j] = in ? v[j] * a.inv_tau : -INFINITY;
+    sc[j] = in ? row_score(a, m, v[j], f[j]) : -INFINITY;
     mx = fmaxf(mx, v[j]);
-    if (idx_of(j) < a.V_high && key_beats(v[j], f[j], bv, bi)) { bv = v[j]; bi = f[j]; }
+    if (in && key_beats(sc[j], f[j], bv, bi)) { bv = sc[j]; bi = f[j]; }
   }
   float se = 0.f;
   if (mx > -INFINITY) {
@@ -321,9 +339,12 @@ __global__ void __launch_bounds__(kRowThreads)
     }
 #pragma unroll
   for (int j = 0; j < kRowVals; ++j) {
-    if (idx_of(j) < a.V_high && !key_beats(T_v, T_i, v[j], f[j])) {
+    if (idx_of(j) < a.V_high && !key_beats(T_v, T_i, sc[j], f[j])) {
       const int p = atomicAdd(&s_cnt, 1);
-      if (p < kRowSurvivors) surv[p] = make_float2(v[j], __int_as_float(f[j]));
+      if (p < kRowSurvivors) {
+        surv[p] = make_float2(sc[j], __int_as_float(f[j]));
+        surv_s[p] = v[j];
+      }
     }
   }
   __syncthreads();
@@ -333,6 +354,7 @@ __global__ void __launch_bounds__(kRowThreads)
   for (int r = tid; r < k; r += kRowThreads) {
     mypart[2 + r] = -INFINITY;
     reinterpret_cast<int*>(mypart)[2 + k + r] = INT_MAX;
+    mypart[2 + 2 * k + r] = -INFINITY;
   }
   __syncthreads();
   for (int c = tid; c < S; c += kRowThreads) {
@@ -343,6 +365,7 @@ __global__ void __launch_bounds__(kRowThreads)
     if (rank < k) {
       mypart[2 + rank] = x;
       reinterpret_cast<int*>(mypart)[2 + k + rank] = i;
+      mypart[2 + 2 * k + rank] = surv_s[c];
     }
   }
   if (tid == 0) { mypart[0] = cm; mypart[1] = cs; }
@@ -369,6 +392,7 @@ __global__ void __launch_bounds__(kRowThreads)
     const float x = __ldcg(rp + (size_t)b * ps + 2 + r);
     const int i = __ldcg(reinterpret_cast<const int*>(rp + (size_t)b * ps) + 2 + k + r);
     surv[c] = make_float2(x, __int_as_float(i));
+    surv_s[c] = __ldcg(rp + (size_t)b * ps + 2 + 2 * k + r);
   }
   __syncthreads();
   int32_t* ids = a.out_ids + (size_t)m * k;
@@ -381,7 +405,7 @@ __global__ void __launch_bounds__(kRowThreads)
     for (int q = 0; q < nc; ++q) rank += key_beats(surv[q].x, __float_as_int(surv[q].y), x, i);
     if (rank < k) {
       ids[rank] = i;
-      probs[rank] = expf(x - mg) / sg;
+      probs[rank] = expf(surv_s[c] - mg) / sg;
     }
   }
   if (tid == 0) a.tickets[m] = 0u;
@@ -432,7 +456,7 @@ static TcLayout tc_layout(int M, int V_high, int k) {
   TcLayout L;
   L.tickets = kHeadRowTicketOffset;
   L.part = kHeadTicketBytes;
-  L.logits = L.part + round256((size_t)M * row_parts(V_high) * (2 + 2 * k) * 4);
+  L.logits = L.part + round256((size_t)M * row_parts(V_high) * (2 + 3 * k) * 4);
   L.total = L.logits + (size_t)M * V_high * 4;
   return L;
 }
@@ -443,8 +467,9 @@ size_t head_tc_workspace(int M, int V_high, int k) {
 
 vt_status head_tc(const uint16_t* H, int M, int d, int64_t ldh,
                   const uint16_t* W, int V_high, const int32_t* t2f, int k,
-                  int32_t* out_ids, float* out_probs, float* out_logits,
-                  void* ws, const DeviceInfo& di, cudaStream_t s) {
+                  const HeadOpts& opt, int32_t* out_ids, float* out_probs,
+                  float* out_logits, void* ws, const DeviceInfo& di,
+                  cudaStream_t s) {
   if (M > 256) return fail(VT_ERR_UNSUPPORTED, "head_tc: M > 256");
   const TcLayout L = tc_layout(M, V_high, k);
   char* wsb = static_cast<char*>(ws);
@@ -463,6 +488,7 @@ vt_status head_tc(const uint16_t* H, int M, int d, int64_t ldh,
   while (cols < (uint32_t)(2 * a.NB)) cols <<= 1;
   a.tmem_cols = cols;
   a.logits = logits;
+  a.bias = opt.bias;
   a.err = err;
   const int stage_bytes = kTcABytes + a.N * kTcBlockK * 2;
   a.stages = std::min<int>(kTcMaxStages, (di.max_smem_optin - 4096) / stage_bytes);
@@ -488,6 +514,10 @@ vt_status head_tc(const uint16_t* H, int M, int d, int64_t ldh,
   r.out_probs = out_probs;
   r.tickets = reinterpret_cast<unsigned*>(wsb + L.tickets);
   r.part = reinterpret_cast<float*>(wsb + L.part);
+  r.inv_tau = 1.0f / opt.tau;
+  r.sample = opt.sample;
+  r.seed = opt.seed;
+  r.offset = opt.offset;
   rows_topk_kernel<<<dim3(P, M), kRowThreads, 0, s>>>(r);
   return launch_status("rows_topk_kernel");
 }

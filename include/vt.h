@@ -126,6 +126,20 @@ vt_status vt_gather_rows(const uint16_t* W, int64_t V, int32_t d,
                          uint64_t* n_invalid, void* stream);
 
 /* ------------------------------------------------------------------------
+ * vt_gather_bias — the kept rows' bias.  [VT] Step 3 copies the old head's
+ * bias with the kept ids when the head has one: b_high[i] = b[t2f[i]].
+ *
+ *   b         (device) float[V], 4-byte aligned.
+ *   t2f       (device) int32[V_high].
+ *   b_high    (device) float[V_high], must not overlap b.
+ *   n_invalid (device, nullable) uint64[1]; accumulated: entries whose t2f
+ *             id lies outside [0, V); they are written as 0.
+ * ------------------------------------------------------------------------ */
+vt_status vt_gather_bias(const float* b, int64_t V, const int32_t* t2f,
+                         int32_t V_high, float* b_high, uint64_t* n_invalid,
+                         void* stream);
+
+/* ------------------------------------------------------------------------
  * vt_draft_head — one draft step of the trimmed head for M hidden states.
  * [FR] Key design: the draft lm_head projects onto the V_high kept rows only
  * and the softmax is taken over that subset; [VT] Step 4: softmax of the
@@ -136,7 +150,7 @@ vt_status vt_gather_rows(const uint16_t* W, int64_t V, int32_t d,
  *   p[m][i]     = exp(logit[m][i] - max_i) / sum_i exp(logit[m][i] - max_i)
  *   out         = the k largest logits of row m, in descending order;
  *                 out_ids = t2f[i] (full-vocabulary ids), out_probs = p.
- *   Equal logits are ordered by lower trimmed index.
+ *   Equal logits are ordered by lower full-vocabulary id.
  *
  *   H         (device) bf16, M rows of d values, row stride ldh elements
  *             (ldh >= d, ldh % 8 == 0), 16-byte aligned.
@@ -170,6 +184,72 @@ vt_status vt_draft_head(const uint16_t* H, int32_t M, int32_t d, int64_t ldh,
                         const int32_t* t2f, int32_t k, int32_t* out_ids,
                         float* out_probs, float* out_logits, void* ws,
                         size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * vt_draft_head_ex — vt_draft_head with options: a bias on the kept rows,
+ * a temperature, and drawing from the trimmed distribution instead of
+ * taking its top-k.  [VT] Step 3 copies the optional bias of the kept rows
+ * with the weight rows (b_high = b[t2f], gathered by the caller); [VT] Step 4
+ * draws the draft token from the trimmed softmax with multinomial.  Draws
+ * here use the Gumbel-max rule, which draws from the same distribution:
+ *
+ *   logit[m][i] = sum_j H[m][j] * W_high[i][j] + bias_high[i]
+ *   s[m][i]     = logit[m][i] / temperature
+ *   p[m][i]     = exp(s[m][i] - max_i s) / sum_i exp(s[m][i] - max_i s)
+ *   score       = s                         (VT_HEAD_TOPK)
+ *               = s + g(seed, offset, m, t2f[i])   (VT_HEAD_SAMPLE)
+ *   out         = the k largest scores of row m, descending (ties: lower
+ *                 full id); out_ids = full ids, out_probs = their p,
+ *                 out_logits = logit (bias included, before temperature).
+ *
+ * In VT_HEAD_SAMPLE mode, k = 1 is one draw from p and k > 1 is k draws
+ * without replacement.  g is Gumbel noise from the counter-based generator
+ * Philox4x32-10 (Salmon et al., SC 2011): x = word 0 of the block at counter
+ * (full id, m, offset low 32 bits, offset high 32 bits) and key (seed low,
+ * seed high); u = ((x >> 9) + 0.5) / 2^23; g = -log(-log(u)).  Noise is
+ * keyed by the full-vocabulary id, so it does not depend on which tokens
+ * were kept: whenever the untrimmed head's draw (same seed, offset, m) is a
+ * kept token, the trimmed head draws that same token.  Callers advance
+ * `offset` once per draft step; m is the hidden state's row in this call.
+ *
+ *   opts      (host, nullable) options; NULL means no bias, temperature 1,
+ *             VT_HEAD_TOPK (exactly vt_draft_head).
+ *             bias_high   (device, nullable) float[V_high], 4-byte aligned.
+ *             temperature finite and > 0.
+ *             mode        VT_HEAD_TOPK or VT_HEAD_SAMPLE.
+ *             seed, offset generator key and step counter (sampling only).
+ *   Other arguments, the workspace (same size function) and the error word
+ *   are those of vt_draft_head; invalid options return VT_ERR_INVALID_ARG.
+ * ------------------------------------------------------------------------ */
+typedef enum { VT_HEAD_TOPK = 0, VT_HEAD_SAMPLE = 1 } vt_head_mode;
+
+typedef struct {
+  const float* bias_high;
+  float temperature;
+  int32_t mode;
+  uint64_t seed;
+  uint64_t offset;
+} vt_head_options;
+
+vt_status vt_draft_head_ex(const uint16_t* H, int32_t M, int32_t d,
+                           int64_t ldh, const uint16_t* W_high,
+                           int32_t V_high, const int32_t* t2f, int32_t k,
+                           const vt_head_options* opts, int32_t* out_ids,
+                           float* out_probs, float* out_logits, void* ws,
+                           size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * vt_draft_noise — the Gumbel noise g(seed, offset, m, id) that
+ * vt_draft_head_ex adds in VT_HEAD_SAMPLE mode, for n full-vocabulary ids;
+ * for verifying draws.  The pages have no counterpart; it is the same
+ * device function the sampling kernels call.
+ *
+ *   full_ids  (device) int32[n];  out (device) float[n];  n >= 0, m >= 0.
+ *   Stream-ordered and asynchronous.
+ * ------------------------------------------------------------------------ */
+vt_status vt_draft_noise(uint64_t seed, uint64_t offset, int32_t m,
+                         const int32_t* full_ids, int64_t n, float* out,
+                         void* stream);
 
 /* ------------------------------------------------------------------------
  * vt_draft_head_noalloc — vt_draft_head for callers that cannot allocate.

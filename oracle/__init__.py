@@ -63,10 +63,12 @@ def _load():
                                           p, p, p, p, p, p]
         u64, f64 = ctypes.c_uint64, ctypes.c_double
         lib.oracle_philox4x32_10.argtypes = [p, p, p]
+        lib.oracle_gather_bias.argtypes = [p, i64, p, i32, p]
+        lib.oracle_gather_bias.restype = i64
         lib.oracle_gumbel_noise.argtypes = [u64, u64, i32, p, i64, p]
         lib.oracle_draft_head_ex.argtypes = [p, i32, i32, i64, p, i32, p, p,
-                                             f64, i32, u64, u64, i32, p, p, p,
-                                             p, p, p, p]
+                                             f64, i32, u64, u64, i32, i32, p,
+                                             p, p, p, p, p, p]
         for fn in (lib.oracle_count_tokens, lib.oracle_select_vocab,
                    lib.oracle_gather_rows, lib.oracle_head_logits,
                    lib.oracle_draft_head, lib.oracle_philox4x32_10,
@@ -132,6 +134,16 @@ def gather_rows(W, t2f):
     return out, rc
 
 
+def gather_bias(b, t2f):
+    """b_high[i] = b[t2f[i]] (fp32) -> (b_high, number of ids out of range)."""
+    b = np.ascontiguousarray(b, dtype=np.float32)
+    t2f = np.ascontiguousarray(t2f, dtype=np.int32)
+    out = np.empty(t2f.size, dtype=np.float32)
+    bad = _load().oracle_gather_bias(_ptr(b), b.size, _ptr(t2f), t2f.size,
+                                     _ptr(out))
+    return out, int(bad)
+
+
 def head_logits(H, W_high):
     """fp64 logits[M, V_high] = H . W_high^T from bf16 bit patterns."""
     H = _u16(H)
@@ -193,9 +205,10 @@ def gumbel_noise(seed: int, offset: int, m: int, full_ids):
 
 
 def draft_head_ex(H, W_high, t2f, k: int, bias=None, temperature=1.0,
-                  sample=False, seed=0, offset=0):
+                  sample=False, seed=0, offset=0, m_base=0):
     """Draft step with options: optional kept-row bias (fp32), temperature,
-    top-k or Gumbel-max sampling (k draws without replacement).
+    top-k or Gumbel-max sampling (k draws without replacement); the noise of
+    row j uses hidden-state index m_base + j.
 
     Returns dict with ids[M,k], probs[M,k], scores[M,k] (selection keys),
     logits[M,k], trimmed[M,k], row_max[M] (of logit/T), row_sumexp[M].
@@ -220,7 +233,7 @@ def draft_head_ex(H, W_high, t2f, k: int, bias=None, temperature=1.0,
     rc = _load().oracle_draft_head_ex(
         _ptr(H), M, d, d, _ptr(W_high), V_high, _ptr(t2f), _ptr(bias),
         ctypes.c_double(temperature), 1 if sample else 0,
-        ctypes.c_uint64(seed), ctypes.c_uint64(offset), k, _ptr(ids),
+        ctypes.c_uint64(seed), ctypes.c_uint64(offset), m_base, k, _ptr(ids),
         _ptr(probs), _ptr(scores), _ptr(logits), _ptr(trimmed), _ptr(rmax),
         _ptr(rsum))
     if rc:

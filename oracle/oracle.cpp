@@ -183,6 +183,25 @@ int oracle_gather_rows(const uint16_t* W, int64_t V, int32_t d,
   return rc;
 }
 
+// Bias of the kept rows.  [VT] Step 3 copies the old head's bias with the
+// kept ids (new_bias[i] = old_bias[trimmed_to_full[i]]) when the head has
+// one.  b_high[i] = b[t2f[i]]; ids outside [0, V) give 0.  Returns the
+// number of such ids.
+int64_t oracle_gather_bias(const float* b, int64_t V, const int32_t* t2f,
+                           int32_t V_high, float* b_high) {
+  int64_t bad = 0;
+  for (int32_t i = 0; i < V_high; ++i) {
+    const int64_t src = t2f[i];
+    if (src < 0 || src >= V) {
+      b_high[i] = 0.0f;
+      ++bad;
+      continue;
+    }
+    b_high[i] = b[src];
+  }
+  return bad;
+}
+
 // Trimmed projection.  [FR] Key design: the draft LM head projects onto the
 // V_high kept rows only (weight d x 128k -> d x 32k); [VT] Step 4 runs the
 // reconstructed Linear.  logits[m][i] = sum_j H[m][j] * W_high[i][j], every
@@ -275,7 +294,8 @@ int oracle_gumbel_noise(uint64_t seed, uint64_t offset, int32_t m,
 //              rows only, in double;
 //   select   : mode 0 (top-k): the k largest s_i; mode 1 (sample): the k
 //              largest s_i + g_i with g_i = gumbel_noise(seed, offset, m,
-//              full id of i): one draw from p for k = 1 (Gumbel-max), k
+//              full id of i) (m counted from m_base, the row of the first
+//              hidden state in the caller's batch): one draw from p for k = 1 (Gumbel-max), k
 //              draws without replacement for k > 1; ties in either key go
 //              to the lower full id; descending;
 //   remap    : trimmed index -> full id through t2f (nullptr = identity).
@@ -286,7 +306,7 @@ int oracle_draft_head_ex(const uint16_t* H, int32_t M, int32_t d, int64_t ldh,
                          const uint16_t* W_high, int32_t V_high,
                          const int32_t* t2f, const float* bias_high,
                          double temperature, int32_t mode, uint64_t seed,
-                         uint64_t offset, int32_t k, int32_t* ids,
+                         uint64_t offset, int32_t m_base, int32_t k, int32_t* ids,
                          double* probs, double* scores, double* top_logits,
                          int32_t* trimmed_idx, double* row_max,
                          double* row_sumexp) {
@@ -309,7 +329,7 @@ int oracle_draft_head_ex(const uint16_t* H, int32_t M, int32_t d, int64_t ldh,
     double sumexp = 0.0;
     for (int32_t i = 0; i < V_high; ++i) sumexp += std::exp(s[i] - mx);
     for (int32_t i = 0; i < V_high; ++i)
-      key[i] = s[i] + (mode == 1 ? gumbel_noise(seed, offset, m, full_id(i)) : 0.0);
+      key[i] = s[i] + (mode == 1 ? gumbel_noise(seed, offset, m_base + m, full_id(i)) : 0.0);
 
     for (int32_t i = 0; i < V_high; ++i) order[i] = i;
     std::partial_sort(order.begin(), order.begin() + k, order.end(),

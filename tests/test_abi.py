@@ -52,7 +52,7 @@ def test_workspace_sizes(lib):
     assert lib.vt_count_tokens_workspace_size(128256) >= 128256
     assert lib.vt_select_vocab_workspace_size(128256) >= 16 * 128256
     assert lib.vt_draft_head_workspace_size(1, 32768, 10) > 256
-    # the tensor-core path (M >= 5) keeps the [M, V_high] fp32 logits
+    # the tensor-core path (M >= 2) keeps the [M, V_high] fp32 logits
     assert lib.vt_draft_head_workspace_size(64, 32768, 10) >= 64 * 32768 * 4
     assert lib.vt_draft_head_workspace_size(0, 32768, 10) == 0
 
@@ -108,3 +108,47 @@ def test_python_binding_refuses_cpu_tensors():
     with pytest.raises(TypeError):
         vt.draft_head(torch.zeros(1, 8, dtype=torch.bfloat16),
                       torch.zeros(4, 8, dtype=torch.bfloat16), None, 1)
+
+
+def test_draft_head_ex_rejects_bad_options(lib):
+    """Temperature must be finite and positive, the mode known, the bias
+    4-byte aligned; all checked on the host, nothing launched."""
+    ws_ok = lib.vt_draft_head_workspace_size(1, 4096, 10)
+
+    def call(opts):
+        return lib.vt_draft_head_ex(FAKE, 1, 256, 256, FAKE, 4096, None, 10,
+                                    ctypes.byref(opts) if opts else None,
+                                    FAKE, FAKE, None, FAKE, ws_ok, None)
+
+    bad = [vt.HeadOptions(None, 0.0, 0, 0, 0),
+           vt.HeadOptions(None, -1.0, 0, 0, 0),
+           vt.HeadOptions(None, float("nan"), 0, 0, 0),
+           vt.HeadOptions(None, float("inf"), 1, 0, 0),
+           vt.HeadOptions(None, 1.0, 2, 0, 0),
+           vt.HeadOptions(FAKE + 2, 1.0, 0, 0, 0)]
+    for opts in bad:
+        assert call(opts) == INVALID
+    # the head's own argument checks still apply under options
+    opts = vt.HeadOptions(None, 1.0, 1, 7, 0)
+    assert lib.vt_draft_head_ex(FAKE, 1, 256, 256, FAKE, 4096, None, 0,
+                                ctypes.byref(opts), FAKE, FAKE, None, FAKE,
+                                ws_ok, None) == INVALID
+    assert lib.vt_draft_head_ex(FAKE, 1, 256, 256, FAKE, 4096, None, 10,
+                                ctypes.byref(opts), FAKE, FAKE, None, FAKE,
+                                ws_ok - 16, None) == WORKSPACE
+
+
+def test_draft_noise_rejects_bad_arguments(lib):
+    assert lib.vt_draft_noise(1, 2, 0, FAKE, -1, FAKE, None) == INVALID
+    assert lib.vt_draft_noise(1, 2, -1, FAKE, 5, FAKE, None) == INVALID
+    assert lib.vt_draft_noise(1, 2, 0, None, 5, FAKE, None) == INVALID
+    assert lib.vt_draft_noise(1, 2, 0, None, 0, None, None) == OK
+
+
+def test_gather_bias_rejects_bad_arguments(lib):
+    assert lib.vt_gather_bias(None, 10, FAKE, 5, FAKE, None, None) == INVALID
+    assert lib.vt_gather_bias(FAKE, 0, FAKE, 5, FAKE + 4096, None, None) == INVALID
+    assert lib.vt_gather_bias(FAKE + 2, 10, FAKE, 5, FAKE + 4096, None, None) == INVALID
+    # b_high overlapping b
+    assert lib.vt_gather_bias(FAKE, 100, FAKE + 8192, 50, FAKE + 40, None,
+                              None) == INVALID

@@ -174,3 +174,18 @@ def test_vocab_build_full_scale_1e9_tokens():
     assert np.array_equal(f2t.cpu().numpy(), ref["f2t"])
     assert vt.coverage(sums) == ref["coverage"]
     assert 0.93 < ref["coverage"] < 0.95
+
+
+def test_gather_bias_ragged_with_invalid_ids():
+    dev = need_cuda()
+    rng = np.random.default_rng(5)
+    V, V_high = 70001, 3333
+    b = rng.normal(0, 1, V).astype(np.float32)
+    t2f_h = rng.permutation(V)[:V_high].astype(np.int32)
+    t2f_h[[0, 17, V_high - 1]] = [-5, V, 2**31 - 1]
+    n_invalid = torch.zeros(1, dtype=torch.int64, device=dev)
+    out = vt.gather_bias(torch.from_numpy(b).to(dev),
+                         torch.from_numpy(t2f_h).to(dev), n_invalid=n_invalid)
+    ref, bad = oracle.gather_bias(b, t2f_h)
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+    assert int(n_invalid.item()) == bad == 3

@@ -50,12 +50,13 @@ OPTION_MUTANTS = {
                      "logits[i] += 0.0;"),
     "philox_no_key_bump": ("k[0] += kWeyl0;", "k[0] += 0u;"),
     "philox_swapped_halves": ("c[1] = lo1;", "c[1] = lo0;"),
-    "noise_by_trimmed_index": ("gumbel_noise(seed, offset, m, full_id(i))",
-                               "gumbel_noise(seed, offset, m, i)"),
+    "noise_by_trimmed_index": ("gumbel_noise(seed, offset, m_base + m, full_id(i))",
+                               "gumbel_noise(seed, offset, m_base + m, i)"),
     "noise_ignores_row": ("static_cast<uint32_t>(full_id), static_cast<uint32_t>(m),",
                           "static_cast<uint32_t>(full_id), 0u,"),
     "noise_ignores_offset_high": ("static_cast<uint32_t>(offset >> 32)};",
                                   "0u};"),
+    "bias_gather_wrong_index": ("b_high[i] = b[src];", "b_high[i] = b[i];"),
     "sample_prob_of_score": ("if (probs) probs[o] = std::exp(s[i] - mx) / sumexp;\n      if (scores)",
                              "if (probs) probs[o] = std::exp(key[i] - mx) / sumexp;\n      if (scores)"),
 }

@@ -179,3 +179,19 @@ def test_steps_and_seeds_change_the_draw(oracle_lib):
                   oracle.gumbel_noise(1 << 32, 0, 0, ids),
                   oracle.gumbel_noise(1, 0, 1, ids)):
         assert abs(np.corrcoef(a, other)[0, 1]) < 0.1
+
+
+def test_bias_gather_vs_fancy_index(oracle_lib):
+    """b_high = b[t2f] (numpy fancy indexing); out-of-range ids give 0 and
+    are counted."""
+    rng = np.random.default_rng(21)
+    b = rng.normal(0, 1, 500).astype(np.float32)
+    t2f = rng.permutation(500)[:123].astype(np.int32)
+    out, bad = oracle.gather_bias(b, t2f)
+    assert bad == 0 and np.array_equal(out, b[t2f])
+    t2f[[3, 50]] = [-1, 500]
+    out, bad = oracle.gather_bias(b, t2f)
+    assert bad == 2 and out[3] == 0 and out[50] == 0
+    keep = np.ones(123, bool)
+    keep[[3, 50]] = False
+    assert np.array_equal(out[keep], b[t2f[keep]])
