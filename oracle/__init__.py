@@ -64,6 +64,9 @@ def _load():
         u64, f64 = ctypes.c_uint64, ctypes.c_double
         lib.oracle_philox4x32_10.argtypes = [p, p, p]
         lib.oracle_gather_bias.argtypes = [p, i64, p, i32, p]
+        lib.oracle_draft_q.argtypes = [p, i32, i32, i64, p, i32, p, p, f64,
+                                       i32, p]
+        lib.oracle_draft_q.restype = ctypes.c_int
         lib.oracle_gather_bias.restype = i64
         lib.oracle_gumbel_noise.argtypes = [u64, u64, i32, p, i64, p]
         lib.oracle_draft_head_ex.argtypes = [p, i32, i32, i64, p, i32, p, p,
@@ -240,3 +243,23 @@ def draft_head_ex(H, W_high, t2f, k: int, bias=None, temperature=1.0,
         raise ValueError(f"oracle_draft_head_ex: bad arguments (rc={rc})")
     return dict(ids=ids, probs=probs, scores=scores, logits=logits,
                 trimmed=trimmed, row_max=rmax, row_sumexp=rsum)
+
+
+def draft_q(H, W_high, t2f, V: int, bias=None, temperature=1.0):
+    """Full-vocabulary draft distribution q[M, V]: the trimmed softmax at the
+    kept ids (through t2f), 0 at dropped ids."""
+    H = _u16(H)
+    W_high = _u16(W_high)
+    M, d = H.shape
+    V_high = W_high.shape[0]
+    if t2f is not None:
+        t2f = np.ascontiguousarray(t2f, dtype=np.int32)
+    if bias is not None:
+        bias = np.ascontiguousarray(bias, dtype=np.float32)
+    q = np.empty((M, V), dtype=np.float64)
+    rc = _load().oracle_draft_q(_ptr(H), M, d, d, _ptr(W_high), V_high,
+                                _ptr(t2f), _ptr(bias),
+                                ctypes.c_double(temperature), V, _ptr(q))
+    if rc:
+        raise ValueError(f"oracle_draft_q: bad arguments (rc={rc})")
+    return q

@@ -352,4 +352,43 @@ int oracle_draft_head_ex(const uint16_t* H, int32_t M, int32_t d, int64_t ldh,
   return 0;
 }
 
+// Full-vocabulary draft distribution of one draft step.  [FR] Method > Key
+// design: only the draft step changes; verification still uses the full
+// target model and accepts or rejects draft tokens so that the output
+// follows the target's distribution exactly (rejection sampling), which
+// compares the target's and the draft's probabilities over the whole
+// vocabulary.  The trimmed draft gives dropped ids probability 0:
+//   q[m][f] = p[m][i] if f = t2f[i] (a kept id), 0 otherwise,
+// with p the softmax((logit + bias) / T) over the kept rows (as in
+// oracle_draft_head_ex).  q is [M][V]; t2f == nullptr is the identity
+// (V == V_high).
+int oracle_draft_q(const uint16_t* H, int32_t M, int32_t d, int64_t ldh,
+                   const uint16_t* W_high, int32_t V_high, const int32_t* t2f,
+                   const float* bias_high, double temperature, int32_t V,
+                   double* q) {
+  if (M < 0 || d <= 0 || V_high <= 0 || V < V_high || !(temperature > 0.0))
+    return 1;
+  if (!t2f && V != V_high) return 1;
+  std::vector<double> s(static_cast<size_t>(V_high));
+  for (int32_t m = 0; m < M; ++m) {
+    oracle_head_logits(H + static_cast<int64_t>(m) * ldh, 1, d, ldh, W_high,
+                       V_high, s.data());
+    for (int32_t i = 0; i < V_high; ++i)
+      s[i] = (s[i] + (bias_high ? static_cast<double>(bias_high[i]) : 0.0)) /
+             temperature;
+    double mx = s[0];
+    for (int32_t i = 1; i < V_high; ++i) mx = std::max(mx, s[i]);
+    double sumexp = 0.0;
+    for (int32_t i = 0; i < V_high; ++i) sumexp += std::exp(s[i] - mx);
+    double* qm = q + static_cast<int64_t>(m) * V;
+    for (int32_t f = 0; f < V; ++f) qm[f] = 0.0;
+    for (int32_t i = 0; i < V_high; ++i) {
+      const int32_t f = t2f ? t2f[i] : i;
+      if (f < 0 || f >= V) return 2;
+      qm[f] = std::exp(s[i] - mx) / sumexp;
+    }
+  }
+  return 0;
+}
+
 }  // extern "C"

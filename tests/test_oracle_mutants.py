@@ -57,6 +57,10 @@ OPTION_MUTANTS = {
     "noise_ignores_offset_high": ("static_cast<uint32_t>(offset >> 32)};",
                                   "0u};"),
     "bias_gather_wrong_index": ("b_high[i] = b[src];", "b_high[i] = b[i];"),
+    "q_placed_by_position": ("      const int32_t f = t2f ? t2f[i] : i;\n      if (f < 0 || f >= V) return 2;",
+                             "      const int32_t f = i;\n      if (f < 0 || f >= V) return 2;"),
+    "q_without_temperature": ("             temperature;\n    double mx = s[0];",
+                              "             1.0;\n    double mx = s[0];"),
     "sample_prob_of_score": ("if (probs) probs[o] = std::exp(s[i] - mx) / sumexp;\n      if (scores)",
                              "if (probs) probs[o] = std::exp(key[i] - mx) / sumexp;\n      if (scores)"),
 }

@@ -195,3 +195,48 @@ def test_bias_gather_vs_fancy_index(oracle_lib):
     keep = np.ones(123, bool)
     keep[[3, 50]] = False
     assert np.array_equal(out[keep], b[t2f[keep]])
+
+
+def test_draft_q_closed_form(oracle_lib):
+    """q is scipy's softmax((H.W^T + b) / T) over the kept rows placed at the
+    kept ids (numpy fancy indexing), exactly 0 elsewhere, and sums to 1."""
+    from scipy.special import softmax as sp_softmax
+    M, d, V, V_high = 4, 40, 700, 230
+    H = synth.normal_bf16((M, d), 1.0, seed=31)
+    W = synth.normal_bf16((V_high, d), 0.1, seed=32)
+    b = np.random.default_rng(33).normal(0, 0.2, V_high).astype(np.float32)
+    t2f = synth.rank_permutation(V, 34)[:V_high].numpy()
+    logits = H.double().numpy() @ W.double().numpy().T + b.astype(np.float64)
+    for T in (1.0, 0.6):
+        q = oracle.draft_q(synth.bf16_bits(H), synth.bf16_bits(W), t2f, V,
+                           bias=b, temperature=T)
+        want = np.zeros((M, V))
+        want[:, t2f] = sp_softmax(logits / T, axis=1)
+        np.testing.assert_allclose(q, want, rtol=1e-12, atol=1e-15)
+        dropped = np.setdiff1d(np.arange(V), t2f)
+        assert np.all(q[:, dropped] == 0.0)
+        for m in range(M):
+            assert abs(math_fsum(q[m]) - 1.0) < 1e-12
+
+
+def test_draft_q_untrimmed_and_drawn_probabilities(oracle_lib):
+    """With the identity map q is the full softmax; the probability the head
+    reports for a drawn token is q at that token."""
+    from scipy.special import softmax as sp_softmax
+    M, d, V = 3, 32, 300
+    H = synth.normal_bf16((M, d), 1.0, seed=41)
+    W = synth.normal_bf16((V, d), 0.2, seed=42)
+    q = oracle.draft_q(synth.bf16_bits(H), synth.bf16_bits(W), None, V,
+                       temperature=0.9)
+    np.testing.assert_allclose(
+        q, sp_softmax((H.double().numpy() @ W.double().numpy().T) / 0.9, axis=1),
+        rtol=1e-12)
+    r = oracle.draft_head_ex(synth.bf16_bits(H), synth.bf16_bits(W), None, 4,
+                             temperature=0.9, sample=True, seed=1, offset=2)
+    for m in range(M):
+        np.testing.assert_allclose(r["probs"][m], q[m, r["ids"][m]], rtol=1e-12)
+
+
+def math_fsum(x):
+    import math
+    return math.fsum(float(v) for v in x)
