@@ -428,6 +428,23 @@ def run_ours(args, world, rank, local):
     sample_per_call = max_over_ranks(sample_secs, world) / sample_steps
     sample_bytes = V_high * d * 2 + M * d * 2 + M * 8
 
+    # ---- the full-vocabulary draft distribution q (verification input)
+    f2t = torch.full((V,), -1, dtype=torch.int32, device=dev)
+    f2t[t2f.long()] = torch.arange(V_high, dtype=torch.int32, device=dev)
+    q_out = {}
+    for Mq in (1, 60):
+        lg = torch.randn(Mq, V_high, device=dev)
+        qbuf = torch.empty(Mq, V, device=dev)
+        ws_q = torch.empty(max(256, 8 * Mq), dtype=torch.uint8, device=dev)
+        t_q = max_over_ranks(graph_seconds(
+            torch, lambda: vt.draft_q(lg, f2t, V, out=qbuf, ws=ws_q), 50),
+            world)
+        q_bytes = Mq * V * 4 + V * 4 + Mq * V_high * 4 * 2
+        q_out[f"M={Mq}"] = {"us_per_call": t_q * 1e6,
+                            "hbm_gbs": q_bytes / t_q / 1e9,
+                            "frac": q_bytes / t_q / 1e9 / peak}
+        del lg, qbuf
+
     out = {
         "metric": METRIC, "value": value, "unit": "calls/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -464,6 +481,8 @@ def run_ours(args, world, rank, local):
             "achieved_gbs": sample_bytes / sample_per_call / 1e9,
             "frac": sample_bytes / sample_per_call / 1e9 / peak,
         },
+        "draft_q": dict(q_out, note="q[M, 128256] from [M, 32768] logits; "
+                        "bytes = q write + f2t + logits read twice (L2)"),
         "full_vocab": {
             "V": V, "us_per_call": full_per_call * 1e6,
             "calls_per_s": 1.0 / full_per_call,

@@ -87,6 +87,9 @@ def load(build_if_missing: bool = True):
                                   p], ctypes.c_int),
             "vt_draft_noise": ([ctypes.c_uint64, ctypes.c_uint64, i32, p, i64,
                                 p, p], ctypes.c_int),
+            "vt_draft_q_workspace_size": ([i32], sz),
+            "vt_draft_q": ([p, i32, i32, p, i32, ctypes.c_float, p, p, sz, p],
+                           ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -300,6 +303,34 @@ def gather_bias(b: torch.Tensor, t2f: torch.Tensor,
     _check("vt_gather_bias", load().vt_gather_bias(
         _ptr(b), b.numel(), _ptr(t2f), t2f.numel(), _ptr(out), _ptr(n_invalid),
         _stream(dev)))
+    return out
+
+
+def draft_q(logits: torch.Tensor, f2t: torch.Tensor | None, V: int,
+            temperature: float = 1.0, out: torch.Tensor | None = None,
+            ws: torch.Tensor | None = None) -> torch.Tensor:
+    """Full-vocabulary draft distribution q[M, V] from the head's logits
+    [M, V_high] (bias included): softmax(logit / T) at the kept ids (through
+    f2t), 0 at dropped ids; ``f2t=None`` is the identity."""
+    _cuda(logits, "logits", torch.float32)
+    if logits.dim() != 2:
+        raise ValueError("logits must be [M, V_high]")
+    M, V_high = logits.shape
+    dev = logits.device
+    if f2t is not None:
+        _cuda(f2t, "f2t", torch.int32)
+        if f2t.numel() != V:
+            raise ValueError("f2t must hold V entries")
+    if out is None:
+        out = torch.empty(M, V, dtype=torch.float32, device=dev)
+    _cuda(out, "out", torch.float32)
+    lib = load()
+    nbytes = lib.vt_draft_q_workspace_size(M)
+    if ws is None:
+        ws = _ws.get("draft_q", nbytes, dev, zeroed=False)
+    _check("vt_draft_q", lib.vt_draft_q(
+        _ptr(logits), M, V_high, _ptr(f2t), V, float(temperature), _ptr(out),
+        _ptr(ws), ws.numel(), _stream(dev)))
     return out
 
 

@@ -252,6 +252,34 @@ vt_status vt_draft_noise(uint64_t seed, uint64_t offset, int32_t m,
                          void* stream);
 
 /* ------------------------------------------------------------------------
+ * vt_draft_q — the full-vocabulary draft distribution of a draft step, for
+ * verification.  [FR] Method > Key design: only the draft step is trimmed;
+ * the target model verifies with its accept/reject test (rejection
+ * sampling), which keeps the output exactly the target's distribution and
+ * compares target and draft probabilities over the whole vocabulary, where
+ * the trimmed draft gives every dropped id probability 0:
+ *
+ *   q[m][f] = exp(logits[m][f2t[f]] / T - max) / sum   if f2t[f] >= 0
+ *           = 0                                        otherwise,
+ *   max, sum over the V_high kept logits of row m (softmax of logit / T).
+ *
+ *   logits    (device) float[M, V_high], 4-byte aligned: the head's logits
+ *             (vt_draft_head / _ex out_logits, bias included).
+ *   f2t       (device, nullable) int32[V] from vt_select_vocab; NULL means
+ *             the identity (requires V == V_high).
+ *   V         full vocabulary size, V >= V_high; 1 <= M <= 65535.
+ *   temperature  finite and > 0 (the head's T).
+ *   q         (device) float[M, V], 4-byte aligned (16-byte aligned rows
+ *             and V % 4 == 0 take the vector path), must not overlap logits.
+ *   ws        (device) vt_draft_q_workspace_size(M) bytes, 8-byte aligned;
+ *             holds per-row (max, sum); no zero-fill needed.
+ * ------------------------------------------------------------------------ */
+size_t vt_draft_q_workspace_size(int32_t M);
+vt_status vt_draft_q(const float* logits, int32_t M, int32_t V_high,
+                     const int32_t* f2t, int32_t V, float temperature,
+                     float* q, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * vt_draft_head_noalloc — vt_draft_head for callers that cannot allocate.
  * The pages have no counterpart to this call; it exists for integration.
  *

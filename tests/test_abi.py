@@ -152,3 +152,26 @@ def test_gather_bias_rejects_bad_arguments(lib):
     # b_high overlapping b
     assert lib.vt_gather_bias(FAKE, 100, FAKE + 8192, 50, FAKE + 40, None,
                               None) == INVALID
+
+
+def test_draft_q_rejects_bad_arguments(lib):
+    ws = lib.vt_draft_q_workspace_size(4)
+    assert ws == 32 and lib.vt_draft_q_workspace_size(0) == 0
+    good = dict(logits=FAKE, M=4, V_high=100, f2t=FAKE + 65536, V=500, T=1.0,
+                q=FAKE + 131072, ws=FAKE + 262144, nbytes=ws)
+
+    def call(**kw):
+        a = dict(good, **kw)
+        return lib.vt_draft_q(a["logits"], a["M"], a["V_high"], a["f2t"], a["V"],
+                              a["T"], a["q"], a["ws"], a["nbytes"], None)
+
+    assert call(logits=None) == INVALID
+    assert call(M=0) == INVALID
+    assert call(V=99) == INVALID
+    assert call(f2t=None) == INVALID          # identity needs V == V_high
+    assert call(T=0.0) == INVALID
+    assert call(T=float("nan")) == INVALID
+    assert call(q=FAKE + 2) == INVALID        # misaligned and overlapping
+    assert call(q=FAKE + 400) == INVALID      # overlaps logits
+    assert call(nbytes=ws - 8) == WORKSPACE
+    assert call(ws=None) == WORKSPACE
