@@ -110,6 +110,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = tmem_base;
+  // the per-row kernel (a programmatic dependent) may become resident now;
+  // it waits for this grid's completion before reading the logits
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp == 0) {
     if (lane == 0) {  // ---------------------------------- TMA producer
@@ -252,7 +255,11 @@ __device__ __forceinline__ float row_score(const RowArgs& a, int m, float s, int
   return a.sample ? s + gumbel_noise(a.seed, a.offset, m, f) : s;
 }
 
-__global__ void __launch_bounds__(kRowThreads)
+// At most 64 registers a thread, so four CTAs share an SM and a launch of
+// up to 4 * SMs CTAs runs in one wave.  Launched as a programmatic
+// dependent of the GEMM: its CTAs may be resident early and wait for the
+// logits in griddepcontrol.wait.
+__global__ void __launch_bounds__(kRowThreads, 4)
     rows_topk_kernel(RowArgs a) {
   constexpr int kWarps = kRowThreads / 32;
   __shared__ float red[kWarps];
@@ -261,6 +268,7 @@ __global__ void __launch_bounds__(kRowThreads)
   __shared__ float2 surv[kRowSurvivors];  // (score, full id)
   __shared__ float surv_s[kRowSurvivors]; // logit / T of the survivor
   __shared__ int s_cnt, s_last;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int m = blockIdx.y, part_idx = blockIdx.x, k = a.k;
   const int ps = 2 + 3 * k;
@@ -475,9 +483,6 @@ vt_status head_tc(const uint16_t* H, int M, int d, int64_t ldh,
   char* wsb = static_cast<char*>(ws);
   unsigned* err = reinterpret_cast<unsigned*>(wsb + 128);
   float* logits = out_logits ? out_logits : reinterpret_cast<float*>(wsb + L.logits);
-  const int P = row_parts(V_high);
-  if (P * k > kRowSurvivors)
-    return fail(VT_ERR_UNSUPPORTED, "head_tc: V_high * k too large for the row merge");
   TcArgs a;
   a.V_high = V_high;
   a.d = d;
@@ -504,6 +509,9 @@ vt_status head_tc(const uint16_t* H, int M, int d, int64_t ldh,
   head_tc_gemm_kernel<<<grid, kTcThreads, smem, s>>>(tmW, tmH, a);
   vt_status st = launch_status("head_tc_gemm_kernel");
   if (st != VT_OK) return st;
+  const int P = row_parts(V_high);
+  if (P * k > kRowSurvivors)
+    return fail(VT_ERR_UNSUPPORTED, "head_tc: V_high * k too large for the row merge");
   RowArgs r;
   r.logits = logits;
   r.V_high = V_high;
@@ -518,7 +526,18 @@ vt_status head_tc(const uint16_t* H, int M, int d, int64_t ldh,
   r.sample = opt.sample;
   r.seed = opt.seed;
   r.offset = opt.offset;
-  rows_topk_kernel<<<dim3(P, M), kRowThreads, 0, s>>>(r);
+  // a programmatic dependent of the GEMM: launched (and possibly resident)
+  // early; each CTA waits for the GEMM's logits in griddepcontrol.wait
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(P, M);
+  cfg.blockDim = dim3(kRowThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, rows_topk_kernel, r);
   return launch_status("rows_topk_kernel");
 }
 
