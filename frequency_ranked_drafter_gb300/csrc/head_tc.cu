@@ -234,7 +234,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 constexpr int kRowThreads = 256;
 constexpr int kRowVals = 16;
 constexpr int kRowSpan = kRowThreads * kRowVals;  // 4096 logits per CTA
-constexpr int kRowSurvivors = 2048;
+// Survivors of one CTA: every value of its span can survive in the worst
+// case (a span's values at or above T number at most k per warp's threads
+// times kRowVals, which for k = 32 is the whole span), so the buffer holds
+// the span.
+constexpr int kRowSurvivors = kRowSpan;
+constexpr int kRowSmem = kRowSurvivors * (sizeof(float2) + sizeof(float));
 
 struct RowArgs {
   const float* logits;  // [M][V_high], bias already added
@@ -265,8 +270,8 @@ __global__ void __launch_bounds__(kRowThreads, 4)
   __shared__ float red[kWarps];
   __shared__ float tw_v[kWarps];
   __shared__ int tw_i[kWarps];
-  __shared__ float2 surv[kRowSurvivors];  // (score, full id)
-  __shared__ float surv_s[kRowSurvivors]; // logit / T of the survivor
+  extern __shared__ __align__(16) float2 surv[];  // [kRowSurvivors] (score, full id)
+  float* surv_s = reinterpret_cast<float*>(surv + kRowSurvivors);  // logit / T
   __shared__ int s_cnt, s_last;
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -531,12 +536,14 @@ vt_status head_tc(const uint16_t* H, int M, int d, int64_t ldh,
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(P, M);
   cfg.blockDim = dim3(kRowThreads);
+  cfg.dynamicSmemBytes = kRowSmem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (!allow_max_smem(rows_topk_kernel, di)) return VT_ERR_CUDA;
   cudaLaunchKernelEx(&cfg, rows_topk_kernel, r);
   return launch_status("rows_topk_kernel");
 }

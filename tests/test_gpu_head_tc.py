@@ -121,3 +121,29 @@ def test_gemv_and_tc_paths_share_one_workspace():
         ref = oracle.draft_head(Hh, Wh, None, k)
         check_topk(ids.cpu().numpy(), probs.cpu().numpy(),
                    oracle.head_logits(Hh, Wh), None, ref, k)
+
+
+def test_tc_row_survivor_worst_case_k32():
+    """k = 32 with one low-scoring thread in every warp of a row part: the
+    part's bound T is then low and nearly every value of the 4096-value part
+    survives it; all of them must be ranked (none dropped), so the ids equal
+    the oracle's exactly (logits exact: one-hot hidden states)."""
+    dev = need_cuda()
+    V_high, d, M, k = 8192, 64, 3, 32
+    rng = np.random.default_rng(90)
+    vals = 1.0 + rng.integers(0, 128, V_high) / 128.0  # bf16-exact
+    i = np.arange(V_high)
+    t = ((i % 4096) % 1024) // 4  # thread of the part holding index i
+    vals[t % 32 == 0] = -5.0
+    W = np.zeros((V_high, d), np.float32)
+    W[:, 0] = vals
+    Hn = np.zeros((M, d), np.float32)
+    Hn[:, 0] = 1.0
+    Wd = torch.from_numpy(W).to(torch.bfloat16).to(dev)
+    Hd = torch.from_numpy(Hn).to(torch.bfloat16).to(dev)
+    t2f = synth.rank_permutation(2 * V_high, 91)[:V_high].to(dev)
+    ids, probs = vt.draft_head(Hd, Wd, t2f, k)
+    torch.cuda.synchronize()
+    ref = oracle.draft_head(bits_host(Hd), bits_host(Wd), t2f.cpu().numpy(), k)
+    assert np.array_equal(ids.cpu().numpy(), ref["ids"])
+    np.testing.assert_allclose(probs.cpu().numpy(), ref["probs"], atol=1e-6)
