@@ -308,6 +308,49 @@ __device__ __forceinline__ void warp_top_heads(const List& list, int b0, int b1,
   oy = y[0];
 }
 
+// Same for 32 < b1 - b0 <= 64 heads, of which only the k best need to be
+// exact: the first 32 are sorted in registers, then the others that beat
+// the list's k-th key (ballot; few) are inserted one at a time, the last lane
+// dropping out.  The list stays sorted and holds only real heads, and its
+// first k entries are the share's k best: enough for cta_merge_lists to
+// give the k best of all.
+template <class List>
+__device__ __forceinline__ void warp_top_heads_ins(const List& list, int b0, int b1,
+                                                   int k, entry_key& ox, int& oy) {
+  const int lane = threadIdx.x & 31;
+  entry_key x[1];
+  int y[1];
+  {
+    const int b = b0 + lane;
+    x[0] = b < b1 ? list(b)[0] : kEmptyKey;
+    y[0] = b < b1 ? b : -1;
+  }
+  const int b = b0 + 32 + lane;
+  const entry_key x1 = b < b1 ? list(b)[0] : kEmptyKey;  // loaded before the sort
+  warp_bitonic_desc<1>(x, y);
+  entry_key thr = __shfl_sync(~0u, x[0], k - 1);
+  unsigned cand = __ballot_sync(~0u, x1 > thr);
+  while (cand) {  // warp-uniform
+    const int src = __ffs(cand) - 1;
+    const entry_key ck = __shfl_sync(~0u, x1, src);
+    const int p = __popc(__ballot_sync(~0u, x[0] > ck));
+    const entry_key up = __shfl_up_sync(~0u, x[0], 1);
+    const int upy = __shfl_up_sync(~0u, y[0], 1);
+    if (lane == p) {
+      x[0] = ck;
+      y[0] = b0 + 32 + src;
+    } else if (lane > p) {
+      x[0] = up;
+      y[0] = upy;
+    }
+    thr = __shfl_sync(~0u, x[0], k - 1);
+    cand &= ~(1u << src);
+    cand &= __ballot_sync(~0u, x1 > thr);
+  }
+  ox = x[0];
+  oy = y[0];
+}
+
 // Merge of all CTAs' partial results, run by the last CTA of a launch
 // (NT threads, W = NT/32 warps).  Each CTA published (max, sumexp) and its
 // k best entries as sorted keys, so for every hidden state m:
@@ -382,7 +425,7 @@ __device__ void head_final_merge(const HeadArgs& a, int MR, int G, float* stage,
       const int L = (G + W - 1) / W;
       const int b0 = warp * L, b1 = min(G, b0 + L);
       if (L <= 32) warp_top_heads<1>(list, b0, b1, hx, hy);
-      else if (L <= 64) warp_top_heads<2>(list, b0, b1, hx, hy);
+      else if (L <= 64) warp_top_heads_ins(list, b0, b1, k, hx, hy);
       else warp_top_heads<kSortE>(list, b0, b1, hx, hy);
     }
     // the k best heads of all, in order (distinct: lists hold disjoint ids);
