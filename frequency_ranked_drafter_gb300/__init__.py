@@ -372,6 +372,63 @@ def draft_head_host(H_host: torch.Tensor, W_high: torch.Tensor,
     return ids_host, probs_host
 
 
+class HostDraftHead:
+    """Draft steps from host memory, each one CUDA-graph replay: the copy of
+    the step's hidden states to the device, the head, and one copy of the
+    ids and probabilities back (packed in one buffer), then a synchronise.
+
+    ``W_high``, ``t2f``, ``k``, M, d and the options (bias, temperature) are
+    fixed at construction; drawing (``sample=True``) is not offered here,
+    because a replayed graph repeats its step counter.  ``head(H_host)``
+    copies ``H_host`` (host, bf16 [M, d]) into the pinned staging buffer
+    ``head.H_host`` (or pass nothing after writing ``head.H_host`` yourself)
+    and returns host views (ids [M, k] int32, probs [M, k] float32) that the
+    next call overwrites."""
+
+    def __init__(self, W_high: torch.Tensor, t2f: torch.Tensor | None, k: int,
+                 M: int, bias: torch.Tensor | None = None,
+                 temperature: float = 1.0):
+        _cuda(W_high, "W_high", torch.bfloat16)
+        dev = W_high.device
+        V_high, d = W_high.shape
+        self.M, self.k = M, k
+        self.H_host = torch.empty((M, d), dtype=torch.bfloat16, pin_memory=True)
+        self.H_host.zero_()
+        self._out_host = torch.empty(2 * M * k, dtype=torch.int32, pin_memory=True)
+        self._H_dev = torch.empty((M, d), dtype=torch.bfloat16, device=dev)
+        self._out_dev = torch.empty(2 * M * k, dtype=torch.int32, device=dev)
+        ids_dev = self._out_dev[:M * k].view(M, k)
+        probs_dev = self._out_dev[M * k:].view(torch.float32).view(M, k)
+        lib = load()
+        self._ws = torch.zeros(lib.vt_draft_head_workspace_size(M, V_high, k),
+                               dtype=torch.uint8, device=dev)
+        self._stream = torch.cuda.Stream(dev)
+
+        def step():
+            self._H_dev.copy_(self.H_host, non_blocking=True)
+            draft_head(self._H_dev, W_high, t2f, k, out_ids=ids_dev,
+                       out_probs=probs_dev, ws=self._ws, bias=bias,
+                       temperature=temperature)
+            self._out_host.copy_(self._out_dev, non_blocking=True)
+
+        with torch.cuda.stream(self._stream):
+            step()  # eager once: kernel attributes, first-call set-up
+        self._stream.synchronize()
+        self._graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self._graph, stream=self._stream):
+            step()
+        self.ids = self._out_host[:M * k].view(M, k)
+        self.probs = self._out_host[M * k:].view(torch.float32).view(M, k)
+
+    def __call__(self, H_host: torch.Tensor | None = None):
+        if H_host is not None:
+            self.H_host.copy_(H_host)
+        with torch.cuda.stream(self._stream):
+            self._graph.replay()
+        self._stream.synchronize()
+        return self.ids, self.probs
+
+
 def build_vocab(tokens: torch.Tensor, V: int, V_high: int,
                 W: torch.Tensor | None = None, b: torch.Tensor | None = None):
     """The offline build in one call: histogram, selection, maps and (if

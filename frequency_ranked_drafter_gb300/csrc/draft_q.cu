@@ -10,11 +10,11 @@
 //   q[m][f] = exp(s[m][f2t[f]] - max_m) / sum_m   if f2t[f] >= 0,  else 0,
 // with s = logit / T over the kept rows (the head's logits, bias included).
 //
-// Two launches: per row, (max, sum of exp) of s over the V_high logits
-// (one CTA per row, online per thread, folded across the block); then the
-// fill, eight consecutive ids per thread: f2t and q move in 16-byte vectors
-// (when aligned), the kept logits are gathered from L2.  The fill is bound
-// by writing q (M * V * 4 bytes).
+// When a row of logits fits in shared memory (V_high <= ~56K): one kernel,
+// each CTA staging its row there (q_row_kernel).  Otherwise two launches:
+// per row, (max, sum of exp) of s (one CTA per row, batched loads), then the
+// fill, eight consecutive ids for four rows per thread with the kept logits
+// gathered from L2.  Both are bound by writing q (M * V * 4 bytes).
 #include <cmath>
 
 #include "vt_common.cuh"
@@ -25,6 +25,7 @@ namespace {
 constexpr int kStatThreads = 1024;
 constexpr int kFillThreads = 256;
 constexpr int kFillIds = 8;  // ids per thread
+constexpr int kFillRows = 4;  // rows per thread
 
 // Folds (m2, s2) into (m, s), pairs of (max, sum of exp(x - max)); empty
 // pairs (-inf, 0) are neutral.
@@ -34,19 +35,52 @@ __device__ __forceinline__ void fold(float& m, float& s, float m2, float s2) {
   m = M;
 }
 
+// Row statistics: each thread folds its values of the row online; the
+// loads go out eight 16-byte vectors at a time (or eight scalars when the
+// row is not 16-byte aligned), so one L2 round trip serves 32 values.
 __global__ void __launch_bounds__(kStatThreads)
     q_stats_kernel(const float* __restrict__ logits, int V_high, float inv_tau,
-                   float2* __restrict__ stats) {
+                   float2* __restrict__ stats, bool vec) {
   __shared__ float wm[kStatThreads / 32], wsum[kStatThreads / 32];
   const float* row = logits + (size_t)blockIdx.x * V_high;
   float m = -INFINITY, s = 0.f;
-  for (int i = threadIdx.x; i < V_high; i += kStatThreads) {
-    const float x = __ldcg(row + i) * inv_tau;
+  auto add = [&](float x) {
+    if (x == -INFINITY) return;  // padding
+    x *= inv_tau;
     if (x > m) {
       s = (s > 0.f ? s * expf(m - x) : 0.f) + 1.f;
       m = x;
     } else {
       s += expf(x - m);
+    }
+  };
+  constexpr int kBatch = 8;
+  if (vec) {
+    const float4* r4 = reinterpret_cast<const float4*>(row);
+    const int n4 = V_high / 4;
+    for (int base = 0; base < n4; base += kStatThreads * kBatch) {
+      float4 v[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int i = base + j * kStatThreads + threadIdx.x;
+        v[j] = i < n4 ? __ldcg(r4 + i)
+                      : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      }
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        add(v[j].x); add(v[j].y); add(v[j].z); add(v[j].w);
+      }
+    }
+  } else {
+    for (int base = 0; base < V_high; base += kStatThreads * kBatch) {
+      float v[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int i = base + j * kStatThreads + threadIdx.x;
+        v[j] = i < V_high ? __ldcg(row + i) : -INFINITY;
+      }
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) add(v[j]);
     }
   }
 #pragma unroll
@@ -71,49 +105,168 @@ __global__ void __launch_bounds__(kStatThreads)
   }
 }
 
+// Fill: a thread owns eight consecutive full ids for kFillRows rows: one
+// read of their f2t entries serves every row; the kept logits are gathered
+// from L2 and each row's q segment is written with two 16-byte stores (or
+// scalars at a ragged end / unaligned rows).
 __global__ void __launch_bounds__(kFillThreads)
-    q_fill_kernel(const float* __restrict__ logits, int V_high,
+    q_fill_kernel(const float* __restrict__ logits, int M, int V_high,
                   const int32_t* __restrict__ f2t, int V, float inv_tau,
                   const float2* __restrict__ stats, float* __restrict__ q,
                   bool vec) {
-  const int m = blockIdx.y;
-  const float2 st = stats[m];
-  const float inv_sum = 1.f / st.y;
-  const float* row = logits + (size_t)m * V_high;
-  float* qm = q + (size_t)m * V;
   const int f0 = (blockIdx.x * kFillThreads + threadIdx.x) * kFillIds;
   if (f0 >= V) return;
+  const bool full = vec && f0 + kFillIds <= V;
   int idx[kFillIds];
-  if (vec && f0 + kFillIds <= V) {
-    if (f2t) {
+  if (full && f2t) {
+    const int4 a = __ldg(reinterpret_cast<const int4*>(f2t + f0));
+    const int4 b = __ldg(reinterpret_cast<const int4*>(f2t + f0) + 1);
+    idx[0] = a.x; idx[1] = a.y; idx[2] = a.z; idx[3] = a.w;
+    idx[4] = b.x; idx[5] = b.y; idx[6] = b.z; idx[7] = b.w;
+  } else {
+#pragma unroll
+    for (int j = 0; j < kFillIds; ++j)
+      idx[j] = f0 + j < V ? (f2t ? __ldg(f2t + f0 + j) : f0 + j) : -1;
+  }
+  const int m0 = blockIdx.y * kFillRows;
+  float v[kFillRows][kFillIds];
+#pragma unroll
+  for (int r = 0; r < kFillRows; ++r) {
+    const int m = min(m0 + r, M - 1);
+    const float* row = logits + (size_t)m * V_high;
+#pragma unroll
+    for (int j = 0; j < kFillIds; ++j)
+      v[r][j] = (idx[j] >= 0 && idx[j] < V_high) ? __ldcg(row + idx[j]) : -INFINITY;
+  }
+#pragma unroll
+  for (int r = 0; r < kFillRows; ++r) {
+    const int m = m0 + r;
+    if (m >= M) break;
+    const float2 st = stats[m];
+    const float inv_sum = 1.f / st.y;
+    float o[kFillIds];
+#pragma unroll
+    for (int j = 0; j < kFillIds; ++j)
+      o[j] = v[r][j] == -INFINITY ? 0.f : expf(v[r][j] * inv_tau - st.x) * inv_sum;
+    float* qm = q + (size_t)m * V;
+    if (full) {
+      float4* dst = reinterpret_cast<float4*>(qm + f0);
+      dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+      dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < kFillIds; ++j)
+        if (f0 + j < V) qm[f0 + j] = o[j];
+    }
+  }
+}
+
+// One kernel when a row of logits fits in shared memory: grid (P, M); every
+// CTA of row m stages the row's V_high logits in shared memory (coalesced
+// 16-byte loads), folds the row's (max, sum of exp) from there, then fills
+// its 1/P of q[m]: f2t in 16-byte vectors, the kept logits gathered from
+// shared memory (no L2 sector per gathered value), q in 16-byte stores.
+constexpr int kRowQThreads = 1024;
+
+__global__ void __launch_bounds__(kRowQThreads, 1)
+    q_row_kernel(const float* __restrict__ logits, int V_high,
+                 const int32_t* __restrict__ f2t, int V, float inv_tau,
+                 float* __restrict__ q, int span, bool vec) {
+  extern __shared__ __align__(16) float srow[];  // [V_high] logit / T
+  __shared__ float wm[kRowQThreads / 32], wsum[kRowQThreads / 32];
+  __shared__ float2 st_all;
+  const int m = blockIdx.y;
+  const float* row = logits + (size_t)m * V_high;
+  float mm = -INFINITY, ss = 0.f;
+  auto add = [&](float x) {
+    if (x > mm) {
+      ss = (ss > 0.f ? ss * expf(mm - x) : 0.f) + 1.f;
+      mm = x;
+    } else {
+      ss += expf(x - mm);
+    }
+  };
+  if ((V_high & 3) == 0 && (reinterpret_cast<uintptr_t>(row) & 15) == 0) {
+    const float4* r4 = reinterpret_cast<const float4*>(row);
+    float4* s4 = reinterpret_cast<float4*>(srow);
+    const int n4 = V_high / 4;
+    constexpr int kBatch = 8;  // loads in flight per thread
+    for (int base = 0; base < n4; base += kRowQThreads * kBatch) {
+      float4 x[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int i = base + j * kRowQThreads + threadIdx.x;
+        if (i < n4) x[j] = __ldcg(r4 + i);
+      }
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int i = base + j * kRowQThreads + threadIdx.x;
+        if (i < n4) {
+          float4 y = x[j];
+          y.x *= inv_tau; y.y *= inv_tau; y.z *= inv_tau; y.w *= inv_tau;
+          s4[i] = y;
+          add(y.x); add(y.y); add(y.z); add(y.w);
+        }
+      }
+    }
+  } else {
+    for (int i = threadIdx.x; i < V_high; i += kRowQThreads) {
+      const float x = __ldcg(row + i) * inv_tau;
+      srow[i] = x;
+      add(x);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(~0u, mm, o);
+    const float s2 = __shfl_xor_sync(~0u, ss, o);
+    fold(mm, ss, m2, s2);
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) { wm[warp] = mm; wsum[warp] = ss; }
+  __syncthreads();  // also publishes the staged row
+  if (warp == 0) {
+    mm = wm[lane];
+    ss = wsum[lane];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(~0u, mm, o);
+      const float s2 = __shfl_xor_sync(~0u, ss, o);
+      fold(mm, ss, m2, s2);
+    }
+    if (lane == 0) st_all = make_float2(mm, 1.f / ss);
+  }
+  __syncthreads();
+  const float mx = st_all.x, inv_sum = st_all.y;
+  float* qm = q + (size_t)m * V;
+  const int f_begin = blockIdx.x * span, f_end = min(V, f_begin + span);
+  for (int f0 = f_begin + threadIdx.x * kFillIds; f0 < f_end;
+       f0 += kRowQThreads * kFillIds) {
+    int idx[kFillIds];
+    const bool full = vec && f0 + kFillIds <= f_end;
+    if (full && f2t) {
       const int4 a = __ldg(reinterpret_cast<const int4*>(f2t + f0));
       const int4 b = __ldg(reinterpret_cast<const int4*>(f2t + f0) + 1);
       idx[0] = a.x; idx[1] = a.y; idx[2] = a.z; idx[3] = a.w;
       idx[4] = b.x; idx[5] = b.y; idx[6] = b.z; idx[7] = b.w;
     } else {
 #pragma unroll
-      for (int j = 0; j < kFillIds; ++j) idx[j] = f0 + j;
+      for (int j = 0; j < kFillIds; ++j)
+        idx[j] = f0 + j < f_end ? (f2t ? __ldg(f2t + f0 + j) : f0 + j) : -1;
     }
-  } else {
+    float o[kFillIds];
 #pragma unroll
     for (int j = 0; j < kFillIds; ++j)
-      idx[j] = f0 + j < V ? (f2t ? __ldg(f2t + f0 + j) : f0 + j) : -1;
-  }
-  float v[kFillIds];
+      o[j] = (idx[j] >= 0 && idx[j] < V_high) ? expf(srow[idx[j]] - mx) * inv_sum : 0.f;
+    if (full) {
+      float4* dst = reinterpret_cast<float4*>(qm + f0);
+      dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+      dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+    } else {
 #pragma unroll
-  for (int j = 0; j < kFillIds; ++j)
-    v[j] = (idx[j] >= 0 && idx[j] < V_high) ? __ldcg(row + idx[j]) : -INFINITY;
-#pragma unroll
-  for (int j = 0; j < kFillIds; ++j)
-    v[j] = v[j] == -INFINITY ? 0.f : expf(v[j] * inv_tau - st.x) * inv_sum;
-  if (vec && f0 + kFillIds <= V) {
-    float4* dst = reinterpret_cast<float4*>(qm + f0);
-    dst[0] = make_float4(v[0], v[1], v[2], v[3]);
-    dst[1] = make_float4(v[4], v[5], v[6], v[7]);
-  } else {
-#pragma unroll
-    for (int j = 0; j < kFillIds; ++j)
-      if (f0 + j < V) qm[f0 + j] = v[j];
+      for (int j = 0; j < kFillIds; ++j)
+        if (f0 + j < f_end) qm[f0 + j] = o[j];
+    }
   }
 }
 
@@ -149,15 +302,30 @@ extern "C" vt_status vt_draft_q(const float* logits, int32_t M, int32_t V_high,
   if (!current_device(&di)) return VT_ERR_CUDA;
   cudaStream_t s = (cudaStream_t)stream;
   const float inv_tau = 1.0f / temperature;
-  float2* stats = static_cast<float2*>(ws);
-  q_stats_kernel<<<M, kStatThreads, 0, s>>>(logits, V_high, inv_tau, stats);
-  vt_status st = launch_status("q_stats_kernel");
-  if (st != VT_OK) return st;
   // 16-byte vectors when every row of q and f2t starts 16-byte aligned
   const bool vec = (V % 4 == 0) && aligned(q, 16) && (!f2t || aligned(f2t, 16));
+  const size_t row_bytes = (size_t)V_high * sizeof(float);
+  if (row_bytes + 1024 <= (size_t)di.max_smem_optin) {
+    // P parts per row: one wave of CTAs (one fits an SM), at least 1024 ids
+    // a part, spans that are whole multiples of the vector width
+    const int want = std::max(1, di.num_sms / M);
+    const int per_part_min = 1024;
+    const int P = std::max(1, std::min(want, (V + per_part_min - 1) / per_part_min));
+    int span = (V + P - 1) / P;
+    span = (span + kFillIds - 1) / kFillIds * kFillIds;
+    if (!allow_max_smem(q_row_kernel, di)) return VT_ERR_CUDA;
+    q_row_kernel<<<dim3((V + span - 1) / span, M), kRowQThreads, row_bytes, s>>>(
+        logits, V_high, f2t, V, inv_tau, q, span, vec);
+    return launch_status("q_row_kernel");
+  }
+  float2* stats = static_cast<float2*>(ws);
+  const bool vrow = (V_high % 4 == 0) && aligned(logits, 16);
+  q_stats_kernel<<<M, kStatThreads, 0, s>>>(logits, V_high, inv_tau, stats, vrow);
+  vt_status st = launch_status("q_stats_kernel");
+  if (st != VT_OK) return st;
   const int per_block = kFillThreads * kFillIds;
-  dim3 grid((V + per_block - 1) / per_block, M);
-  q_fill_kernel<<<grid, kFillThreads, 0, s>>>(logits, V_high, f2t, V, inv_tau,
-                                              stats, q, vec);
+  dim3 grid((V + per_block - 1) / per_block, (M + kFillRows - 1) / kFillRows);
+  q_fill_kernel<<<grid, kFillThreads, 0, s>>>(logits, M, V_high, f2t, V,
+                                              inv_tau, stats, q, vec);
   return launch_status("q_fill_kernel");
 }

@@ -178,3 +178,20 @@ def test_tree_draft_m60_sampled_rows():
     cfg = synth.TREE_HEAD
     run_case(cfg.d, cfg.V_high, cfg.M, cfg.k, seed=cfg.seed, V=cfg.V,
              want_logits=False, check_rows=[0, 17, 31, 48, 59])
+
+
+def test_host_draft_head_graph_steps():
+    """HostDraftHead: each call copies new host hidden states in, replays
+    the captured step and returns the same ids and probabilities as a direct
+    device call on those hidden states (both head paths)."""
+    dev = need_cuda()
+    W = synth.normal_bf16((20000, 1024), 0.02, seed=81, device=dev)
+    t2f = synth.rank_permutation(40000, 82)[:20000].to(dev)
+    for M in (1, 6):
+        head = vt.HostDraftHead(W, t2f, 10, M)
+        for step in range(3):
+            H = synth.normal_bf16((M, 1024), 1.0, seed=83 + step + 10 * M)
+            ids_h, probs_h = head(H)
+            ids_d, probs_d = vt.draft_head(H.to(dev), W, t2f, 10)
+            assert torch.equal(ids_h, ids_d.cpu())
+            torch.testing.assert_close(probs_h, probs_d.cpu(), rtol=1e-6, atol=1e-7)
