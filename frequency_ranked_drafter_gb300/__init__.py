@@ -88,6 +88,10 @@ def load(build_if_missing: bool = True):
             "vt_draft_noise": ([ctypes.c_uint64, ctypes.c_uint64, i32, p, i64,
                                 p, p], ctypes.c_int),
             "vt_draft_q_workspace_size": ([i32], sz),
+            "vt_draft_head_sets_workspace_size": ([i32, i32, i32, i32, p], sz),
+            "vt_draft_head_sets": ([p, i32, i32, i64, p, i32, p, p, p, p, i32,
+                                    ctypes.POINTER(HeadOptions), p, p, p, sz, p],
+                                   ctypes.c_int),
             "vt_draft_q": ([p, i32, i32, p, i32, ctypes.c_float, p, p, sz, p],
                            ctypes.c_int),
         }
@@ -304,6 +308,54 @@ def gather_bias(b: torch.Tensor, t2f: torch.Tensor,
         _ptr(b), b.numel(), _ptr(t2f), t2f.numel(), _ptr(out), _ptr(n_invalid),
         _stream(dev)))
     return out
+
+
+def draft_head_sets(H: torch.Tensor, set_of_row, W_high_sets, t2f_sets, k: int,
+                    bias_sets=None, temperature: float = 1.0,
+                    sample: bool = False, seed: int = 0, offset: int = 0,
+                    out_ids: torch.Tensor | None = None,
+                    out_probs: torch.Tensor | None = None,
+                    ws: torch.Tensor | None = None):
+    """One draft step where hidden state m uses kept vocabulary set
+    ``set_of_row[m]`` (``W_high_sets[s]``, ``t2f_sets[s]``, optional
+    ``bias_sets[s]``); otherwise as draft_head."""
+    if not (isinstance(H, torch.Tensor) and H.is_cuda and H.dtype == torch.bfloat16
+            and H.dim() == 2 and H.stride(1) == 1):
+        raise TypeError("H must be a CUDA bf16 [M, d] tensor with unit column stride")
+    M, d = H.shape
+    S = len(W_high_sets)
+    rows = [int(x) for x in set_of_row]
+    if len(rows) != M:
+        raise ValueError("set_of_row must name a set for every hidden state")
+    for s_, W in enumerate(W_high_sets):
+        _cuda(W, f"W_high_sets[{s_}]", torch.bfloat16)
+    dev = H.device
+    P = ctypes.c_void_p
+    W_arr = (P * S)(*[W.data_ptr() for W in W_high_sets])
+    V_arr = (ctypes.c_int32 * S)(*[W.shape[0] for W in W_high_sets])
+    T_arr = (P * S)(*[None if t is None else _cuda(t, "t2f", torch.int32).data_ptr()
+                      for t in (t2f_sets or [None] * S)])
+    B_arr = None
+    if bias_sets is not None:
+        B_arr = (P * S)(*[None if b is None else _cuda(b, "bias", torch.float32).data_ptr()
+                          for b in bias_sets])
+    sor = (ctypes.c_int32 * M)(*rows)
+    if out_ids is None:
+        out_ids = torch.empty(M, k, dtype=torch.int32, device=dev)
+    if out_probs is None:
+        out_probs = torch.empty(M, k, dtype=torch.float32, device=dev)
+    lib = load()
+    nbytes = lib.vt_draft_head_sets_workspace_size(M, d, k, S, V_arr)
+    if ws is None:
+        ws = _ws.get("head_sets", nbytes, dev, zeroed=True)
+    opts = HeadOptions(None, float(temperature),
+                       VT_HEAD_SAMPLE if sample else VT_HEAD_TOPK,
+                       int(seed) & (2**64 - 1), int(offset) & (2**64 - 1))
+    _check("vt_draft_head_sets", lib.vt_draft_head_sets(
+        _ptr(H), M, d, H.stride(0), sor, S, W_arr, V_arr, T_arr, B_arr, k,
+        ctypes.byref(opts), _ptr(out_ids), _ptr(out_probs), _ptr(ws),
+        ws.numel(), _stream(dev)))
+    return out_ids, out_probs
 
 
 def draft_q(logits: torch.Tensor, f2t: torch.Tensor | None, V: int,

@@ -92,6 +92,45 @@ extern "C" vt_status vt_draft_head(const uint16_t* H, int32_t M, int32_t d,
                              ws_bytes, stream);
 }
 
+namespace vt {
+
+// Checked copy of the public options (NULL = defaults).
+static vt_status head_options(const char* who, const vt_head_options* opts,
+                              HeadOpts* opt) {
+  *opt = HeadOpts{nullptr, 1.0f, 0, 0, 0};
+  if (!opts) return VT_OK;
+  const std::string w(who);
+  if (!(opts->temperature > 0.0f) || !std::isfinite(opts->temperature))
+    return fail(VT_ERR_INVALID_ARG, w + ": temperature must be finite and > 0");
+  if (opts->mode != VT_HEAD_TOPK && opts->mode != VT_HEAD_SAMPLE)
+    return fail(VT_ERR_INVALID_ARG, w + ": unknown mode");
+  if (opts->bias_high && !aligned(opts->bias_high, 4))
+    return fail(VT_ERR_INVALID_ARG, w + ": bias_high not 4B aligned");
+  opt->bias = opts->bias_high;
+  opt->tau = opts->temperature;
+  opt->sample = opts->mode == VT_HEAD_SAMPLE;
+  opt->seed = opts->seed;
+  opt->offset = opts->offset;
+  return VT_OK;
+}
+
+vt_status draft_head_rows(const uint16_t* H, int32_t M, int32_t d, int64_t ldh,
+                          const uint16_t* W_high, int32_t V_high,
+                          const int32_t* t2f, int32_t k,
+                          const vt_head_options* opts, const int32_t* row_ids,
+                          int32_t* out_ids, float* out_probs, void* ws,
+                          size_t ws_bytes, void* stream) {
+  HeadOpts opt;
+  vt_status st = head_options("vt_draft_head_sets", opts, &opt);
+  if (st != VT_OK) return st;
+  opt.row_ids = row_ids;
+  return draft_head_impl("vt_draft_head_sets", H, M, d, ldh, W_high, V_high,
+                         t2f, k, opt, out_ids, out_probs, nullptr, ws, ws_bytes,
+                         stream);
+}
+
+}  // namespace vt
+
 extern "C" vt_status vt_draft_head_ex(const uint16_t* H, int32_t M, int32_t d,
                                       int64_t ldh, const uint16_t* W_high,
                                       int32_t V_high, const int32_t* t2f,
@@ -100,21 +139,9 @@ extern "C" vt_status vt_draft_head_ex(const uint16_t* H, int32_t M, int32_t d,
                                       float* out_logits, void* ws,
                                       size_t ws_bytes, void* stream) {
   using namespace vt;
-  HeadOpts opt{nullptr, 1.0f, 0, 0, 0};
-  if (opts) {
-    if (!(opts->temperature > 0.0f) || !std::isfinite(opts->temperature))
-      return fail(VT_ERR_INVALID_ARG,
-                  "vt_draft_head_ex: temperature must be finite and > 0");
-    if (opts->mode != VT_HEAD_TOPK && opts->mode != VT_HEAD_SAMPLE)
-      return fail(VT_ERR_INVALID_ARG, "vt_draft_head_ex: unknown mode");
-    if (opts->bias_high && !aligned(opts->bias_high, 4))
-      return fail(VT_ERR_INVALID_ARG, "vt_draft_head_ex: bias_high not 4B aligned");
-    opt.bias = opts->bias_high;
-    opt.tau = opts->temperature;
-    opt.sample = opts->mode == VT_HEAD_SAMPLE;
-    opt.seed = opts->seed;
-    opt.offset = opts->offset;
-  }
+  HeadOpts opt;
+  vt_status st = head_options("vt_draft_head_ex", opts, &opt);
+  if (st != VT_OK) return st;
   return draft_head_impl("vt_draft_head_ex", H, M, d, ldh, W_high, V_high,
                          t2f, k, opt, out_ids, out_probs, out_logits, ws,
                          ws_bytes, stream);

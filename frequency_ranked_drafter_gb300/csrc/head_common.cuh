@@ -31,6 +31,8 @@ struct HeadOpts {
   float tau;
   int sample;
   uint64_t seed, offset;
+  const int32_t* row_ids = nullptr;  // device; the noise index of each hidden
+                                     // state of the launch (null: its row)
 };
 
 // Each CTA b publishes, per hidden state m, one record of `pstride` 32-bit
@@ -484,6 +486,15 @@ __device__ void head_final_merge(const HeadArgs& a, int MR, int G, float* stage,
 
 // CUDA-core GEMV path (M = 1 in vt_draft_head; up to 4 per launch), head_gemv.cu.
 vt_status head_gemv(const HeadArgs& a, const DeviceInfo& di, cudaStream_t s);
+
+// vt_draft_head_ex with a device map giving each hidden state's noise index
+// (its row in the caller's batch); the sets entry point uses it (head_api.cu).
+vt_status draft_head_rows(const uint16_t* H, int32_t M, int32_t d, int64_t ldh,
+                          const uint16_t* W_high, int32_t V_high,
+                          const int32_t* t2f, int32_t k,
+                          const vt_head_options* opts, const int32_t* row_ids,
+                          int32_t* out_ids, float* out_probs, void* ws,
+                          size_t ws_bytes, void* stream);
 
 // Tree-draft tensor-core path (M >= kHeadTcMinM), head_tc.cu.  The
 // workspace holds an error word at byte 128, per-row counters and partials

@@ -92,6 +92,10 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
     tk[m] = kEmptyKey; thr[m] = kEmptyKey;
   }
   const float* bias = a.opt.bias;
+  int mrow[MR];  // noise index of each hidden state
+#pragma unroll
+  for (int m = 0; m < MR; ++m)
+    mrow[m] = a.opt.row_ids ? __ldg(a.opt.row_ids + a.m_base + m) : a.m_base + m;
   const float inv_tau = 1.0f / a.opt.tau;
 
   const int nchunks = d >> 3;
@@ -138,7 +142,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
         for (int u = 0; u < U; ++u)
 #pragma unroll
           for (int m = 0; m < MR; ++m)
-            noise[u][m] = gumbel_noise(a.opt.seed, a.opt.offset, a.m_base + m, fid[u]);
+            noise[u][m] = gumbel_noise(a.opt.seed, a.opt.offset, mrow[m], fid[u]);
       }
 #pragma unroll
       for (int j = 0; j < CPL; ++j) {

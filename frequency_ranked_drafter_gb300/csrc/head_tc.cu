@@ -252,12 +252,14 @@ struct RowArgs {
   float inv_tau;  // 1 / T
   int sample;
   uint64_t seed, offset;
+  const int32_t* row_ids;  // noise index of each row (null: the row)
 };
 
 // Selection score of one logit: s = logit / T, plus the token's Gumbel noise
 // when sampling.
 __device__ __forceinline__ float row_score(const RowArgs& a, int m, float s, int f) {
-  return a.sample ? s + gumbel_noise(a.seed, a.offset, m, f) : s;
+  return a.sample ? s + gumbel_noise(a.seed, a.offset, a.row_ids ? __ldg(a.row_ids + m) : m, f)
+                  : s;
 }
 
 // At most 64 registers a thread, so four CTAs share an SM and a launch of
@@ -531,6 +533,7 @@ vt_status head_tc(const uint16_t* H, int M, int d, int64_t ldh,
   r.sample = opt.sample;
   r.seed = opt.seed;
   r.offset = opt.offset;
+  r.row_ids = opt.row_ids;
   // a programmatic dependent of the GEMM: launched (and possibly resident)
   // early; each CTA waits for the GEMM's logits in griddepcontrol.wait
   cudaLaunchConfig_t cfg = {};

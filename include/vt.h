@@ -252,6 +252,44 @@ vt_status vt_draft_noise(uint64_t seed, uint64_t offset, int32_t m,
                          void* stream);
 
 /* ------------------------------------------------------------------------
+ * vt_draft_head_sets — one draft step for hidden states that use different
+ * kept vocabularies.  [FR] Limitations: the kept set is one static,
+ * corpus-wide vocabulary; vocabularies chosen per domain or per request are
+ * future work.  Each set s has its own W_high_sets[s] [V_high_sets[s], d],
+ * t2f_sets[s] and optional bias_sets[s], built by the same offline calls
+ * from its own token stream; hidden state m is scored against set
+ * set_of_row[m] exactly as vt_draft_head_ex would score it alone, and when
+ * drawing its noise index is its row m in this call.
+ *
+ *   H, M (1..256), d, ldh, k, opts, out_ids, out_probs: as vt_draft_head_ex
+ *             (opts->bias_high must be NULL: biases are per set).
+ *   set_of_row  (host) int32[M], 0 <= set_of_row[m] < S.
+ *   W_high_sets (host) array of S device pointers, 16-byte aligned.
+ *   V_high_sets (host) int32[S], each >= k.
+ *   t2f_sets    (host, nullable) array of S device pointers (entries may
+ *               be NULL: identity).
+ *   bias_sets   (host, nullable) array of S device pointers (nullable
+ *               entries), fp32 [V_high_sets[s]], 4-byte aligned.
+ *   ws          (device) vt_draft_head_sets_workspace_size(M, d, k, S,
+ *               V_high_sets) bytes, 256-byte aligned, zero-filled once
+ *               before its first use.
+ * For each set in use: one gather of its rows' hidden states, the head
+ * (GEMV for one row, tensor cores for more), one scatter of its outputs.
+ * All sets are checked before anything is launched.
+ * ------------------------------------------------------------------------ */
+size_t vt_draft_head_sets_workspace_size(int32_t M, int32_t d, int32_t k,
+                                         int32_t S, const int32_t* V_high_sets);
+vt_status vt_draft_head_sets(const uint16_t* H, int32_t M, int32_t d,
+                             int64_t ldh, const int32_t* set_of_row, int32_t S,
+                             const uint16_t* const* W_high_sets,
+                             const int32_t* V_high_sets,
+                             const int32_t* const* t2f_sets,
+                             const float* const* bias_sets, int32_t k,
+                             const vt_head_options* opts, int32_t* out_ids,
+                             float* out_probs, void* ws, size_t ws_bytes,
+                             void* stream);
+
+/* ------------------------------------------------------------------------
  * vt_draft_q — the full-vocabulary draft distribution of a draft step, for
  * verification.  [FR] Method > Key design: only the draft step is trimmed;
  * the target model verifies with its accept/reject test (rejection

@@ -175,3 +175,23 @@ def test_draft_q_rejects_bad_arguments(lib):
     assert call(q=FAKE + 400) == INVALID      # overlaps logits
     assert call(nbytes=ws - 8) == WORKSPACE
     assert call(ws=None) == WORKSPACE
+
+
+def test_draft_head_sets_rejects_bad_arguments(lib):
+    P = ctypes.c_void_p
+    W = (P * 2)(FAKE, FAKE + 1 << 24)
+    V = (ctypes.c_int32 * 2)(100, 200)
+    sor = (ctypes.c_int32 * 3)(0, 1, 0)
+    ws = lib.vt_draft_head_sets_workspace_size(3, 64, 5, 2, V)
+    assert ws > 0 and lib.vt_draft_head_sets_workspace_size(3, 64, 5, 0, V) == 0
+
+    def call(sor=sor, S=2, W=W, V=V, k=5, opts=None, nbytes=ws):
+        return lib.vt_draft_head_sets(FAKE, 3, 64, 64, sor, S, W, V, None, None,
+                                      k, ctypes.byref(opts) if opts else None,
+                                      FAKE, FAKE, FAKE, nbytes, None)
+
+    assert call(sor=(ctypes.c_int32 * 3)(0, 2, 0)) == INVALID   # set out of range
+    assert call(V=(ctypes.c_int32 * 2)(100, 3)) == INVALID      # V_high < k
+    assert call(W=(P * 2)(FAKE, FAKE + 8)) == INVALID           # misaligned W
+    assert call(opts=vt.HeadOptions(FAKE, 1.0, 0, 0, 0)) == INVALID  # bias in opts
+    assert call(nbytes=ws - 256) == WORKSPACE
