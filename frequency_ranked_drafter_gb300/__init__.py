@@ -88,6 +88,12 @@ def load(build_if_missing: bool = True):
             "vt_draft_noise": ([ctypes.c_uint64, ctypes.c_uint64, i32, p, i64,
                                 p, p], ctypes.c_int),
             "vt_draft_q_workspace_size": ([i32], sz),
+            "vt_host_step_create": ([p, i32, i32, p, i32, i32,
+                                     ctypes.POINTER(HeadOptions),
+                                     ctypes.POINTER(p)], ctypes.c_int),
+            "vt_host_step_run": ([p, p, p, p], ctypes.c_int),
+            "vt_host_step_staging": ([p], p),
+            "vt_host_step_destroy": ([p], None),
             "vt_draft_head_sets_workspace_size": ([i32, i32, i32, i32, p], sz),
             "vt_draft_head_sets": ([p, i32, i32, i64, p, i32, p, p, p, p, i32,
                                     ctypes.POINTER(HeadOptions), p, p, p, sz, p],
@@ -425,60 +431,54 @@ def draft_head_host(H_host: torch.Tensor, W_high: torch.Tensor,
 
 
 class HostDraftHead:
-    """Draft steps from host memory, each one CUDA-graph replay: the copy of
-    the step's hidden states to the device, the head, and one copy of the
-    ids and probabilities back (packed in one buffer), then a synchronise.
-
-    ``W_high``, ``t2f``, ``k``, M, d and the options (bias, temperature) are
-    fixed at construction; drawing (``sample=True``) is not offered here,
-    because a replayed graph repeats its step counter.  ``head(H_host)``
-    copies ``H_host`` (host, bf16 [M, d]) into the pinned staging buffer
-    ``head.H_host`` (or pass nothing after writing ``head.H_host`` yourself)
-    and returns host views (ids [M, k] int32, probs [M, k] float32) that the
-    next call overwrites."""
+    """Draft steps from host memory through the library's host step
+    (vt_host_step_*): each call copies the hidden states into the handle's
+    pinned staging buffer, launches one CUDA graph (copy in, the head, one
+    copy of ids and probabilities back), synchronises, and returns host
+    tensors (ids [M, k] int32, probs [M, k] float32) that the next call
+    overwrites.  ``W_high``, ``t2f``, ``k``, M and the options (bias,
+    temperature) are fixed; drawing is not offered (a replayed graph repeats
+    its step counter).  Write ``head.H_host`` in place and call ``head()``
+    to skip the host copy."""
 
     def __init__(self, W_high: torch.Tensor, t2f: torch.Tensor | None, k: int,
                  M: int, bias: torch.Tensor | None = None,
                  temperature: float = 1.0):
         _cuda(W_high, "W_high", torch.bfloat16)
-        dev = W_high.device
+        if t2f is not None:
+            _cuda(t2f, "t2f", torch.int32)
+        if bias is not None:
+            _cuda(bias, "bias", torch.float32)
         V_high, d = W_high.shape
         self.M, self.k = M, k
-        self.H_host = torch.empty((M, d), dtype=torch.bfloat16, pin_memory=True)
-        self.H_host.zero_()
-        self._out_host = torch.empty(2 * M * k, dtype=torch.int32, pin_memory=True)
-        self._H_dev = torch.empty((M, d), dtype=torch.bfloat16, device=dev)
-        self._out_dev = torch.empty(2 * M * k, dtype=torch.int32, device=dev)
-        ids_dev = self._out_dev[:M * k].view(M, k)
-        probs_dev = self._out_dev[M * k:].view(torch.float32).view(M, k)
+        self._keep = (W_high, t2f, bias)  # the graph reads these
         lib = load()
-        self._ws = torch.zeros(lib.vt_draft_head_workspace_size(M, V_high, k),
-                               dtype=torch.uint8, device=dev)
-        self._stream = torch.cuda.Stream(dev)
-
-        def step():
-            self._H_dev.copy_(self.H_host, non_blocking=True)
-            draft_head(self._H_dev, W_high, t2f, k, out_ids=ids_dev,
-                       out_probs=probs_dev, ws=self._ws, bias=bias,
-                       temperature=temperature)
-            self._out_host.copy_(self._out_dev, non_blocking=True)
-
-        with torch.cuda.stream(self._stream):
-            step()  # eager once: kernel attributes, first-call set-up
-        self._stream.synchronize()
-        self._graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(self._graph, stream=self._stream):
-            step()
-        self.ids = self._out_host[:M * k].view(M, k)
-        self.probs = self._out_host[M * k:].view(torch.float32).view(M, k)
+        opts = HeadOptions(_ptr(bias), float(temperature), VT_HEAD_TOPK, 0, 0)
+        h = ctypes.c_void_p()
+        with torch.cuda.device(W_high.device):
+            _check("vt_host_step_create", lib.vt_host_step_create(
+                _ptr(W_high), V_high, d, _ptr(t2f), M, k, ctypes.byref(opts),
+                ctypes.byref(h)))
+        self._h = h
+        staging = lib.vt_host_step_staging(h)
+        buf = (ctypes.c_uint16 * (M * d)).from_address(staging)
+        self.H_host = torch.frombuffer(buf, dtype=torch.int16).view(
+            torch.bfloat16).view(M, d)
+        self.ids = torch.empty(M, k, dtype=torch.int32)
+        self.probs = torch.empty(M, k, dtype=torch.float32)
+        self._lib = lib
 
     def __call__(self, H_host: torch.Tensor | None = None):
-        if H_host is not None:
-            self.H_host.copy_(H_host)
-        with torch.cuda.stream(self._stream):
-            self._graph.replay()
-        self._stream.synchronize()
+        src = self.H_host if H_host is None else H_host.contiguous()
+        _check("vt_host_step_run", self._lib.vt_host_step_run(
+            self._h, src.data_ptr(), self.ids.data_ptr(), self.probs.data_ptr()))
         return self.ids, self.probs
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h:
+            self._lib.vt_host_step_destroy(h)
+            self._h = None
 
 
 def build_vocab(tokens: torch.Tensor, V: int, V_high: int,

@@ -1,0 +1,145 @@
+// vt_host_step_* — a draft step from host memory, replayed from a CUDA graph
+// owned by the library.
+//
+// A caller that keeps its hidden states on the host (a CPU-side decode loop,
+// a different process's buffers) pays per step for: the copy of the step's
+// hidden states to the device, the head, the copy of ids and probabilities
+// back, and a synchronise.  The handle captures the three device operations
+// once (device copy of H from a pinned staging buffer, vt_draft_head_ex, one
+// device-to-host copy of ids and probabilities packed together) into a CUDA
+// graph on its own stream; each step is then a host copy of H into the
+// staging buffer, one graph launch, one synchronise and a host copy out.
+// The pages have no counterpart: it serves the end-to-end use of the head.
+#include <cstring>
+#include <new>
+
+#include "head_common.cuh"
+
+struct vt_host_step {
+  int M, d, k;
+  cudaStream_t stream = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  uint16_t* H_pinned = nullptr;   // host, pinned [M, d]
+  int32_t* out_pinned = nullptr;  // host, pinned [2, M, k] (ids, prob bits)
+  uint16_t* H_dev = nullptr;      // device [M, d]
+  int32_t* out_dev = nullptr;     // device [2, M, k]
+  void* ws = nullptr;             // device head workspace
+};
+
+namespace {
+
+void destroy(vt_host_step* h) {
+  if (!h) return;
+  if (h->exec) cudaGraphExecDestroy(h->exec);
+  if (h->stream) cudaStreamDestroy(h->stream);
+  if (h->H_pinned) cudaFreeHost(h->H_pinned);
+  if (h->out_pinned) cudaFreeHost(h->out_pinned);
+  if (h->H_dev) cudaFree(h->H_dev);
+  if (h->out_dev) cudaFree(h->out_dev);
+  if (h->ws) cudaFree(h->ws);
+  delete h;
+}
+
+}  // namespace
+
+extern "C" vt_status vt_host_step_create(const uint16_t* W_high, int32_t V_high,
+                                         int32_t d, const int32_t* t2f,
+                                         int32_t M, int32_t k,
+                                         const vt_head_options* opts,
+                                         vt_host_step** out) {
+  using namespace vt;
+  if (!out) return fail(VT_ERR_INVALID_ARG, "vt_host_step_create: null handle");
+  *out = nullptr;
+  if (opts && opts->mode == VT_HEAD_SAMPLE)
+    return fail(VT_ERR_INVALID_ARG,
+                "vt_host_step_create: drawing needs a new step counter per call; "
+                "a replayed graph would repeat it");
+  if (!W_high || M < 1 || M > 256 || d < 8 || d % 8 || k < 1 || k > kTopKMax ||
+      V_high < k)
+    return fail(VT_ERR_INVALID_ARG, "vt_host_step_create: bad arguments");
+  vt_host_step* h = new (std::nothrow) vt_host_step;
+  if (!h) return fail(VT_ERR_CUDA, "vt_host_step_create: out of host memory");
+  h->M = M;
+  h->d = d;
+  h->k = k;
+  const size_t hbytes = (size_t)M * d * 2, obytes = (size_t)M * k * 8;
+  const size_t wbytes = vt_draft_head_workspace_size(M, V_high, k);
+  auto bad = [&](const char* what) {
+    const cudaError_t e = cudaGetLastError();
+    destroy(h);
+    return fail(VT_ERR_CUDA, std::string("vt_host_step_create: ") + what + ": " +
+                                 cudaGetErrorString(e));
+  };
+  if (cudaStreamCreateWithFlags(&h->stream, cudaStreamNonBlocking) != cudaSuccess)
+    return bad("stream");
+  if (cudaMallocHost(&h->H_pinned, hbytes) != cudaSuccess ||
+      cudaMallocHost(&h->out_pinned, obytes) != cudaSuccess ||
+      cudaMalloc(&h->H_dev, hbytes) != cudaSuccess ||
+      cudaMalloc(&h->out_dev, obytes) != cudaSuccess ||
+      cudaMalloc(&h->ws, wbytes) != cudaSuccess)
+    return bad("allocation");
+  std::memset(h->H_pinned, 0, hbytes);
+  if (cudaMemsetAsync(h->ws, 0, wbytes, h->stream) != cudaSuccess) return bad("memset");
+  int32_t* ids_dev = h->out_dev;
+  float* probs_dev = reinterpret_cast<float*>(h->out_dev + (size_t)M * k);
+  // one eager step first (kernel attributes, first-call set-up), then capture
+  for (int pass = 0; pass < 2; ++pass) {
+    if (pass == 1 &&
+        cudaStreamBeginCapture(h->stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
+      return bad("begin capture");
+    if (cudaMemcpyAsync(h->H_dev, h->H_pinned, hbytes, cudaMemcpyHostToDevice,
+                        h->stream) != cudaSuccess)
+      return bad("copy in");
+    const vt_status st = vt_draft_head_ex(h->H_dev, M, d, d, W_high, V_high, t2f, k,
+                                          opts, ids_dev, probs_dev, nullptr, h->ws,
+                                          wbytes, h->stream);
+    if (st != VT_OK) {
+      if (pass == 1) {
+        cudaGraph_t g = nullptr;
+        cudaStreamEndCapture(h->stream, &g);
+        if (g) cudaGraphDestroy(g);
+      }
+      destroy(h);
+      return st;
+    }
+    if (cudaMemcpyAsync(h->out_pinned, h->out_dev, obytes, cudaMemcpyDeviceToHost,
+                        h->stream) != cudaSuccess)
+      return bad("copy out");
+    if (pass == 0 && cudaStreamSynchronize(h->stream) != cudaSuccess)
+      return bad("first step");
+  }
+  cudaGraph_t graph = nullptr;
+  if (cudaStreamEndCapture(h->stream, &graph) != cudaSuccess || !graph)
+    return bad("end capture");
+  const cudaError_t ie = cudaGraphInstantiate(&h->exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (ie != cudaSuccess) return bad("instantiate");
+  *out = h;
+  return VT_OK;
+}
+
+extern "C" vt_status vt_host_step_run(vt_host_step* h, const uint16_t* H_host,
+                                      int32_t* ids_host, float* probs_host) {
+  using namespace vt;
+  if (!h || !H_host || !ids_host || !probs_host)
+    return fail(VT_ERR_INVALID_ARG, "vt_host_step_run: null pointer");
+  const size_t mk = (size_t)h->M * h->k;
+  if (H_host != h->H_pinned)
+    std::memcpy(h->H_pinned, H_host, (size_t)h->M * h->d * 2);
+  if (cudaGraphLaunch(h->exec, h->stream) != cudaSuccess ||
+      cudaStreamSynchronize(h->stream) != cudaSuccess)
+    return fail(VT_ERR_CUDA, std::string("vt_host_step_run: ") +
+                                 cudaGetErrorString(cudaGetLastError()));
+  std::memcpy(ids_host, h->out_pinned, mk * 4);
+  std::memcpy(probs_host, h->out_pinned + mk, mk * 4);
+  return VT_OK;
+}
+
+extern "C" uint16_t* vt_host_step_staging(vt_host_step* h) {
+  return h ? h->H_pinned : nullptr;
+}
+
+extern "C" void vt_host_step_destroy(vt_host_step* h) {
+  if (h) cudaStreamSynchronize(h->stream);
+  destroy(h);
+}

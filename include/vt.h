@@ -318,6 +318,36 @@ vt_status vt_draft_q(const float* logits, int32_t M, int32_t V_high,
                      float* q, void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * vt_host_step_* — draft steps from host memory, each one CUDA-graph launch.
+ * The pages have no counterpart; this serves callers whose hidden states
+ * live on the host.  The handle owns a stream, pinned staging buffers,
+ * device buffers, a zero-filled head workspace and a CUDA graph of: copy of
+ * the staged H [M, d] to the device, vt_draft_head_ex, one copy of the ids
+ * and probabilities back.
+ *
+ *   vt_host_step_create: W_high, V_high, d, t2f, M (1..256), k and opts are
+ *     fixed for the handle's life (W_high and t2f must stay valid); opts may
+ *     set a bias and a temperature, not VT_HEAD_SAMPLE (a replayed graph
+ *     would repeat its step counter).  Runs one step eagerly, then captures.
+ *     This call allocates and synchronises; the run call does neither.
+ *   vt_host_step_run: copies H_host (host, bf16 [M, d]; skipped when it is
+ *     the staging buffer) into the staging buffer, launches the graph,
+ *     synchronises the handle's stream and writes ids_host [M, k] and
+ *     probs_host [M, k] (host).  Not thread-safe per handle.
+ *   vt_host_step_staging: the pinned [M, d] staging buffer (write H there to
+ *     skip the host copy).
+ *   vt_host_step_destroy: synchronises and frees everything (NULL is a no-op).
+ * ------------------------------------------------------------------------ */
+typedef struct vt_host_step vt_host_step;
+vt_status vt_host_step_create(const uint16_t* W_high, int32_t V_high, int32_t d,
+                              const int32_t* t2f, int32_t M, int32_t k,
+                              const vt_head_options* opts, vt_host_step** out);
+vt_status vt_host_step_run(vt_host_step* h, const uint16_t* H_host,
+                           int32_t* ids_host, float* probs_host);
+uint16_t* vt_host_step_staging(vt_host_step* h);
+void vt_host_step_destroy(vt_host_step* h);
+
+/* ------------------------------------------------------------------------
  * vt_draft_head_noalloc — vt_draft_head for callers that cannot allocate.
  * The pages have no counterpart to this call; it exists for integration.
  *

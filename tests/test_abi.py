@@ -195,3 +195,19 @@ def test_draft_head_sets_rejects_bad_arguments(lib):
     assert call(W=(P * 2)(FAKE, FAKE + 8)) == INVALID           # misaligned W
     assert call(opts=vt.HeadOptions(FAKE, 1.0, 0, 0, 0)) == INVALID  # bias in opts
     assert call(nbytes=ws - 256) == WORKSPACE
+
+
+def test_host_step_rejects_bad_arguments(lib):
+    """Checked before anything is allocated: no handle, drawing, bad sizes."""
+    h = ctypes.c_void_p()
+    assert lib.vt_host_step_create(FAKE, 1000, 256, None, 1, 10, None, None) == INVALID
+    draw = vt.HeadOptions(None, 1.0, 1, 0, 0)
+    assert lib.vt_host_step_create(FAKE, 1000, 256, None, 1, 10, ctypes.byref(draw),
+                                   ctypes.byref(h)) == INVALID
+    assert lib.vt_host_step_create(FAKE, 5, 256, None, 1, 10, None,
+                                   ctypes.byref(h)) == INVALID   # V_high < k
+    assert lib.vt_host_step_create(FAKE, 1000, 250, None, 1, 10, None,
+                                   ctypes.byref(h)) == INVALID   # d % 8
+    assert not h.value
+    assert lib.vt_host_step_run(None, FAKE, FAKE, FAKE) == INVALID
+    lib.vt_host_step_destroy(None)
