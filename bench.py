@@ -318,6 +318,63 @@ def oracle_head_rate(d, V_high, k, budget_s, seed=1002):
     return 1.0 / (per_row_s * V_high), n * rows, el
 
 
+def _oracle_head_worker(a):
+    """One host process of the all-cores oracle run: waits for the common
+    start time, then runs the oracle head on its own slice until the common
+    end time."""
+    d, V_high, k, t_start, t_end, seed = a
+    import numpy as np
+    import oracle
+    import synth
+    rows = min(V_high, 2048)
+    W = synth.bf16_bits(synth.normal_bf16((rows, d), 0.02, seed))
+    H = synth.bf16_bits(synth.normal_bf16((1, d), 1.0, seed + 1))
+    t2f = np.arange(rows, dtype=np.int32)
+    oracle.draft_head(H, W, t2f, k)
+    while time.time() < t_start:
+        time.sleep(0.01)
+    n = 0
+    while time.time() < t_end:
+        oracle.draft_head(H, W, t2f, k)
+        n += 1
+    return n * rows, time.time()
+
+
+def oracle_head_rate_all_cores(d, V_high, k, budget_s, start_delay_s=20.0):
+    """The same oracle, one process per host core (spawned, so none forks a
+    CUDA context), all running over one common interval; the rate is the
+    rows all finished over the interval from the common start to the last
+    finish."""
+    import multiprocessing as mp
+    n_proc = os.cpu_count() or 1
+    t_start = time.time() + start_delay_s
+    t_end = t_start + budget_s
+    with mp.get_context("spawn").Pool(n_proc) as pool:
+        res = pool.map(_oracle_head_worker,
+                       [(d, V_high, k, t_start, t_end, 1002 + 7 * i)
+                        for i in range(n_proc)])
+    rows = sum(r for r, _ in res)
+    el = max(e for _, e in res) - t_start
+    return rows / el / V_high, n_proc, rows, el
+
+
+def oracle_histogram_rate(V, budget_s, n=1 << 24, seed=1005):
+    """The oracle histogram (hash map, then dense counts) on a bounded
+    Zipf(1.1) stream, repeated for the budget: tokens/s on one core."""
+    import oracle
+    import synth
+    tokens = synth.zipf_tokens(n, V, 1.1, seed=seed).numpy()
+    oracle.count_tokens(tokens[:4096], V)
+    done, t0 = 0, time.perf_counter()
+    while True:
+        oracle.count_tokens(tokens, V)
+        done += n
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return done / el, done, el
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return
@@ -505,6 +562,16 @@ def run_ours(args, world, rank, local):
             "value": rate, "unit": "calls/s", "cores": 1, "kind": "oracle",
             "sample": f"{rows} kept rows of the d=4096 head in {el:.1f} s on "
                       f"one host core, scaled to {V_high} rows per call"}
+        rate, cores, rows, el = oracle_head_rate_all_cores(d, V_high, k, 10.0)
+        out["cpu_baseline_all_cores"] = {
+            "value": rate, "unit": "calls/s", "cores": cores, "kind": "oracle",
+            "sample": f"{rows} kept rows of the d=4096 head in {el:.1f} s, one "
+                      f"process per host core, scaled to {V_high} rows per call"}
+        rate, toks, el = oracle_histogram_rate(V, 10.0)
+        out["cpu_baseline_histogram"] = {
+            "value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{toks} Zipf(1.1) tokens over V={V} counted in "
+                      f"{el:.1f} s on one host core"}
     if rank == 0:
         print(json.dumps(out), flush=True)
 
