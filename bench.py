@@ -522,7 +522,7 @@ def run_ours(args, world, rank, local):
                      "peak_kind": peak_kind,
                      "traffic": committed_traffic(),
                      "alg_bytes_per_launch": alg_bytes,
-                     "kernel": "head_gemv_kernel<1,16,1,false>"},
+                     "kernel": "head_gemv_kernel<1,8,2,false>"},
         "e2e": {"value": e2e_value, "unit": "calls/s",
                 "h2d_bytes_per_step": M * d * 2,
                 "d2h_bytes_per_step": M * k * 8,

@@ -43,6 +43,9 @@ namespace {
 
 constexpr int kTcThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
 constexpr int kTcMaxStages = 6;
+// k-blocks of a CTA's first W_high tile prefetched into L2 before the
+// dependency wait.
+constexpr int kTcPrefetchKBlocks = 32;
 constexpr int kTcBlockK = 64;  // bf16 per K block: 128 bytes, one swizzle row
 constexpr int kTcTileRows = 128;
 constexpr int kTcABytes = kTcTileRows * kTcBlockK * 2;  // 16 KB
@@ -112,12 +115,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t tmem = tmem_base;
   // the per-row kernel (a programmatic dependent) may become resident now;
   // it waits for this grid's completion before reading the logits
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  grid_launch_dependents();
+  // This grid is itself a programmatic dependent of the work ahead of it
+  // (the previous draft step's row kernel, or the layer that wrote H): until
+  // that ends, the producer only asks L2 for the first k-blocks of this
+  // CTA's first W_high tile (weights; the TMA loads that use them come after
+  // the wait).  Nothing else is read, and no logit written, before it.
+  if (warp == 0 && lane == 0 && (int)blockIdx.x < ntiles) {
+    tc::prefetch_tensormap(&tmW);
+    tc::prefetch_tensormap(&tmH);
+    const int npre = min(nkb, kTcPrefetchKBlocks);
+    for (int kb = 0; kb < npre; ++kb)
+      tc::tma_prefetch_l2_2d(&tmW, kb * kTcBlockK, (int)blockIdx.x * kTcTileRows);
+  }
+  grid_dependency_wait();
 
   if (warp == 0) {
     if (lane == 0) {  // ---------------------------------- TMA producer
-      tc::prefetch_tensormap(&tmW);
-      tc::prefetch_tensormap(&tmH);
       int s = 0;
       uint32_t ph = 0;
       int issued = 0;  // loads issued, for the drain on abort
@@ -275,7 +289,10 @@ __global__ void __launch_bounds__(kRowThreads, 4)
   extern __shared__ __align__(16) float2 surv[];  // [kRowSurvivors] (score, full id)
   float* surv_s = reinterpret_cast<float*>(surv + kRowSurvivors);  // logit / T
   __shared__ int s_cnt, s_last;
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  grid_dependency_wait();
+  // the GEMM has ended: the next draft step's GEMM (a programmatic
+  // dependent) may now start its weight prefetch beside this kernel
+  grid_launch_dependents();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int m = blockIdx.y, part_idx = blockIdx.x, k = a.k;
   const int ps = 2 + 3 * k;
@@ -513,7 +530,11 @@ vt_status head_tc(const uint16_t* H, int M, int d, int64_t ldh,
   const int ntiles = (V_high + kTcTileRows - 1) / kTcTileRows;
   const int grid = std::min(ntiles, di.num_sms);
   const int smem = a.stages * stage_bytes + 1024;
-  head_tc_gemm_kernel<<<grid, kTcThreads, smem, s>>>(tmW, tmH, a);
+  // a programmatic dependent of the work ahead of it in the stream
+  const cudaError_t e = launch_dependent(head_tc_gemm_kernel, dim3(grid),
+                                         dim3(kTcThreads), smem, s, tmW, tmH, a);
+  if (e != cudaSuccess)
+    return fail(VT_ERR_CUDA, std::string("head_tc_gemm_kernel: ") + cudaGetErrorString(e));
   vt_status st = launch_status("head_tc_gemm_kernel");
   if (st != VT_OK) return st;
   const int P = row_parts(V_high);
@@ -536,18 +557,11 @@ vt_status head_tc(const uint16_t* H, int M, int d, int64_t ldh,
   r.row_ids = opt.row_ids;
   // a programmatic dependent of the GEMM: launched (and possibly resident)
   // early; each CTA waits for the GEMM's logits in griddepcontrol.wait
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(P, M);
-  cfg.blockDim = dim3(kRowThreads);
-  cfg.dynamicSmemBytes = kRowSmem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   if (!allow_max_smem(rows_topk_kernel, di)) return VT_ERR_CUDA;
-  cudaLaunchKernelEx(&cfg, rows_topk_kernel, r);
+  const cudaError_t e2 = launch_dependent(rows_topk_kernel, dim3(P, M),
+                                          dim3(kRowThreads), kRowSmem, s, r);
+  if (e2 != cudaSuccess)
+    return fail(VT_ERR_CUDA, std::string("rows_topk_kernel: ") + cudaGetErrorString(e2));
   return launch_status("rows_topk_kernel");
 }
 

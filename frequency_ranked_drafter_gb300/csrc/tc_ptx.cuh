@@ -71,6 +71,17 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map,
       : "memory");
 }
 
+// Asks L2 for the box at (x, y) of a tiled tensor map (a hint: nothing is
+// returned and nothing waits on it).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map,
+                                                   int x, int y) {
+  asm volatile(
+      "cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y)
+      : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }

@@ -6,6 +6,7 @@
 
 #include <algorithm>
 #include <string>
+#include <utility>
 
 #include "vt.h"
 
@@ -33,6 +34,25 @@ inline bool aligned(const void* p, size_t a) {
 
 // Maps the result of a kernel launch to a status.
 vt_status launch_status(const char* what);
+
+// Launches `kernel` as a programmatic dependent of the work ahead of it in
+// stream `s` (see grid_dependency_wait below): the kernel may start while
+// the previous kernel finishes and must wait before reading its results.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block,
+                             size_t smem, cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Opts `kernel` in to the device's full dynamic shared memory, once per
 // (kernel, device), so later calls (including ones under stream capture)
@@ -76,6 +96,28 @@ __device__ __forceinline__ int4 ld_stream_i4(const void* p) {
 __device__ __forceinline__ void st_stream_u4(void* p, uint4 v) {
   asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x),
                "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// Programmatic dependent launch (PTX griddepcontrol).  A kernel launched
+// with the programmatic-serialization attribute may start before the kernel
+// ahead of it in the stream has ended; it must read nothing that kernel may
+// write before grid_dependency_wait(), which returns once that kernel has
+// completed and its writes are visible (at once when launched normally).
+// grid_launch_dependents() lets the next such kernel start early.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Asks L2 to fetch `bytes` (a multiple of 16) from a 16-byte-aligned global
+// address.  A hint: it returns nothing and orders nothing, so it is safe even
+// before grid_dependency_wait() (the loads that use the data come later and
+// read L2, where every store lands).
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes)
                : "memory");
 }
 
