@@ -79,13 +79,20 @@ __device__ __noinline__ void settle_wrap(uint32_t old, uint32_t word,
   }
 }
 
+// Pass kinds.  kPadded: one pass over every id with V % 4 == 0; an id
+// outside 0..V-1 is clamped to V, byte 0 of a padding word after the
+// histogram, so a token needs no validity test or select: the padding
+// byte's hits (256 per wrap plus its final value) are the invalid tokens.
+// kSingle: one pass over every id, V % 4 != 0.  kRange: one of several
+// passes over id ranges (ids outside the range belong to other passes).
+constexpr int kPadded = 0, kSingle = 1, kRange = 2;
+
 // Sixteen tokens of one thread.  The sixteen shared-memory atomics issue
 // back to back (their latencies overlap); a token's byte wrapped if its old
-// value was 0xff, and all sixteen checks fold into one predicate, so the
-// rare wraps (once per 256 hits of an id) cost one branch per 16 tokens.
-// kSingle: the pass covers every id (lo = 0, Vr = V), so "in range" and
-// "valid" are the same test.
-template <bool kSingle>
+// value was 0xff, and the checks fold into one bit mask, so the rare wraps
+// (once per 256 hits of an id) cost one branch per 16 tokens.  An id this
+// pass does not count adds 0 (kSingle, kRange), which changes nothing.
+template <int kMode>
 __device__ __forceinline__ void count16(uint32_t* sm, const int4 (&v)[4],
                                         uint32_t lo, uint32_t Vr, uint32_t V,
                                         uint32_t* counts_pass,
@@ -101,14 +108,20 @@ __device__ __forceinline__ void count16(uint32_t* sm, const int4 (&v)[4],
   uint32_t wraps = 0;  // bit j: token j's byte wrapped
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
-    const uint32_t u = kSingle ? t[j] : t[j] - lo;
-    const bool in = u < Vr;
-    const uint32_t sh = (u << 3) & 24u;
-    olds[j] = 0u;
-    if (in) olds[j] = atomicAdd(&sm[u >> 2], 1u << sh);
-    if (in && ((~olds[j] >> sh) & 0xffu) == 0u) wraps |= 1u << j;
-    if (kSingle) invalid += in ? 0u : 1u;
-    else if (lo == 0) invalid += t[j] >= V ? 1u : 0u;
+    if (kMode == kPadded) {
+      const uint32_t u = min(t[j], Vr);
+      const uint32_t sh = (u & 3u) << 3;
+      olds[j] = atomicAdd(&sm[u >> 2], 1u << sh);
+      if (((olds[j] >> sh) & 0xffu) == 0xffu) wraps |= 1u << j;
+    } else {
+      const uint32_t u = kMode == kSingle ? t[j] : t[j] - lo;
+      const bool in = u < Vr;
+      const uint32_t sh = (u & 3u) << 3;
+      olds[j] = atomicAdd(&sm[in ? u >> 2 : 0u], in ? 1u << sh : 0u);
+      if (in && ((olds[j] >> sh) & 0xffu) == 0xffu) wraps |= 1u << j;
+      if (kMode == kSingle) invalid += in ? 0u : 1u;
+      else if (lo == 0) invalid += t[j] >= V ? 1u : 0u;
+    }
   }
   // A warp sees about two wraps per step of 512 tokens, so this loop runs
   // in most steps, but only over the wrapped tokens of each thread.
@@ -119,8 +132,10 @@ __device__ __forceinline__ void count16(uint32_t* sm, const int4 (&v)[4],
 #pragma unroll
     for (int q = 0; q < 16; ++q)
       if (q == j) { tj = t[q]; oj = olds[q]; }
-    const uint32_t u = kSingle ? tj : tj - lo;
-    settle_wrap(oj, u >> 2, u & 3u, counts_pass, Vr, wc);
+    const uint32_t u = kMode == kPadded ? min(tj, Vr)
+                                        : (kMode == kSingle ? tj : tj - lo);
+    if (kMode == kPadded && u == Vr) invalid += 256u;  // the padding byte
+    else settle_wrap(oj, u >> 2, u & 3u, counts_pass, Vr, wc);
   }
 }
 
@@ -140,7 +155,7 @@ __device__ __forceinline__ void count1(uint32_t* sm, uint32_t t, uint32_t lo,
   }
 }
 
-template <bool kSingle>
+template <int kMode>
 __global__ void __launch_bounds__(kCountThreads, 1)
     count_tokens_kernel(const int32_t* __restrict__ tokens, int64_t n,
                         uint32_t V, uint32_t lo, uint32_t Vr,
@@ -175,12 +190,12 @@ __global__ void __launch_bounds__(kCountThreads, 1)
     while (true) {
       const bool more_b = i + step + 3 * stride < n4;
       if (more_b) load4(b, i + step);
-      count16<kSingle>(sm, a, lo, Vr, V, counts_pass, invalid, wc);
+      count16<kMode>(sm, a, lo, Vr, V, counts_pass, invalid, wc);
       i += step;
       if (!more_b) break;
       const bool more_a = i + step + 3 * stride < n4;
       if (more_a) load4(a, i + step);
-      count16<kSingle>(sm, b, lo, Vr, V, counts_pass, invalid, wc);
+      count16<kMode>(sm, b, lo, Vr, V, counts_pass, invalid, wc);
       i += step;
       if (!more_a) break;
     }
@@ -196,6 +211,8 @@ __global__ void __launch_bounds__(kCountThreads, 1)
     count1(sm, (uint32_t)tokens[(n4 << 2) + threadIdx.x], lo, Vr, V,
            counts_pass, invalid, wc);
   __syncthreads();
+  // kPadded: the padding byte's final value adds to the invalid tokens
+  if (kMode == kPadded && threadIdx.x == 0) invalid += sm[Vr >> 2] & 0xffu;
 
   uint32_t* slab = slabs + (size_t)blockIdx.x * words_padded;
   for (int w = threadIdx.x; w < words_padded; w += kCountThreads)
@@ -257,7 +274,9 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-int words_for(uint32_t Vr) { return (int)(((Vr + 3) / 4 + 3) & ~3u); }
+// Histogram words of a pass over Vr ids: one byte per id plus (for a
+// padded pass) the padding word at Vr / 4, rounded up to 16 bytes.
+int words_for(uint32_t Vr) { return (int)((Vr / 4 + 1 + 3) & ~3u); }
 
 }  // namespace
 }  // namespace vt
@@ -288,9 +307,10 @@ extern "C" vt_status vt_count_tokens(const int32_t* tokens, int64_t n,
   DeviceInfo di;
   if (!current_device(&di)) return VT_ERR_CUDA;
   const int ids_per_pass = std::min<int>(
-      kCountMaxIds, ((di.max_smem_optin - (int)sizeof(WrapCache)) / 16) * 16);
-  if (!allow_max_smem(count_tokens_kernel<true>, di) ||
-      !allow_max_smem(count_tokens_kernel<false>, di))
+      kCountMaxIds, ((di.max_smem_optin - (int)sizeof(WrapCache)) / 16) * 16 - 16);
+  if (!allow_max_smem(count_tokens_kernel<kPadded>, di) ||
+      !allow_max_smem(count_tokens_kernel<kSingle>, di) ||
+      !allow_max_smem(count_tokens_kernel<kRange>, di))
     return VT_ERR_CUDA;
   const int G = (int)std::max<int64_t>(
       1, std::min<int64_t>({(int64_t)di.num_sms, (int64_t)kCountMaxCtas,
@@ -301,7 +321,9 @@ extern "C" vt_status vt_count_tokens(const int32_t* tokens, int64_t n,
     const uint32_t Vr = (uint32_t)std::min<int64_t>(ids_per_pass, V - lo);
     const int words = words_for(Vr);
     const bool single = lo == 0 && Vr == (uint32_t)V;
-    auto kern = single ? count_tokens_kernel<true> : count_tokens_kernel<false>;
+    auto kern = !single ? count_tokens_kernel<kRange>
+                : Vr % 4 == 0 ? count_tokens_kernel<kPadded>
+                              : count_tokens_kernel<kSingle>;
     kern<<<G, kCountThreads, words * sizeof(uint32_t), s>>>(
         tokens, n, (uint32_t)V, (uint32_t)lo, Vr, counts,
         reinterpret_cast<unsigned long long*>(n_invalid), slabs, words);

@@ -51,6 +51,21 @@ def test_count_byte_wrap_carry_chains():
     assert got[4:].sum() == 0
 
 
+@pytest.mark.parametrize("V", [4096, 4097])
+def test_count_mostly_invalid_ids(V):
+    """Nine tokens in ten out of range: the invalid count (kept in a padding
+    byte past the histogram when V % 4 == 0) wraps thousands of times per CTA
+    and must still be exact, and no valid count may move."""
+    rng = np.random.default_rng(V)
+    n = 3_000_017
+    tokens = rng.integers(0, V, size=n).astype(np.int32)
+    bad = rng.random(n) < 0.9
+    tokens[bad] = rng.choice(np.array([-1, V, V + 3, np.iinfo(np.int32).min,
+                                       np.iinfo(np.int32).max], dtype=np.int32),
+                             size=int(bad.sum()))
+    _count_and_compare(tokens, V)
+
+
 def test_count_single_hot_id():
     tokens = np.full(3_000_001, 7, dtype=np.int32)
     got = _count_and_compare(tokens, 10)
