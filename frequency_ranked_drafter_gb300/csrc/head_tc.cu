@@ -14,7 +14,8 @@
 // pass over W_high serves every hidden state.  Per CTA (persistent over
 // tiles of 128 rows): warp 0 streams K blocks of 64 (128 bytes, 128-byte
 // swizzle) of the W tile and of H into a ring of shared-memory stages with
-// TMA; one thread of warp 1 issues tcgen05.mma into a double-buffered TMEM
+// TMA (a stage is up to four such K blocks of the same rows, requested back
+// to back); one thread of warp 1 issues tcgen05.mma into a double-buffered TMEM
 // accumulator; warps 2-5 read finished accumulators out of TMEM and store
 // fp32 logits (tile rows along lanes, so every store is a coalesced 128-byte
 // row segment).  At these M the work stays bound by the W_high stream.
@@ -46,7 +47,13 @@ constexpr int kTcMaxStages = 6;
 // k-blocks of a CTA's first W_high tile prefetched into L2 before the
 // dependency wait.
 constexpr int kTcPrefetchKBlocks = 32;
-constexpr int kTcBlockK = 64;  // bf16 per K block: 128 bytes, one swizzle row
+constexpr int kTcBlockK = 64;  // bf16 per K atom: 128 bytes, one swizzle row
+// A stage holds up to kTcMaxAtoms K atoms (adjacent 128-byte pieces of the
+// same 128 W_high rows, loaded back to back), as many as leave kTcMinStages
+// stages: wider stages give DRAM longer runs per row (M = 60, V_high =
+// 32768: 68.5 us with one atom a stage, 59.2 us with two).
+constexpr int kTcMaxAtoms = 4;
+constexpr int kTcMinStages = 3;
 constexpr int kTcTileRows = 128;
 constexpr int kTcABytes = kTcTileRows * kTcBlockK * 2;  // 16 KB
 constexpr long long kWaitBudget = 2000000000LL;
@@ -54,10 +61,16 @@ constexpr long long kWaitBudget = 2000000000LL;
 struct TcArgs {
   int V_high, d, M, N, NB;  // NB: TMEM column stride of one accumulator
   int stages;
+  int atoms;  // K atoms (64 columns, 128 bytes a row) per stage
   uint32_t tmem_cols;
   float* logits;  // [M][V_high]
   const float* bias;  // [V_high] or null, added to every logit
   unsigned* err;
+  // top-k calls: per hidden state m and 32-row quadrant q of the tiles,
+  // (max, sum of exp(s - max)) of s = logit / T, at qstat[m * nq + q]
+  float2* qstat;
+  int nq;
+  float inv_tau;
 };
 
 __device__ __forceinline__ void record_error(unsigned* err, volatile int* abort) {
@@ -77,6 +90,50 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
   return true;
 }
 
+// Reduces, per column j of a 32-column accumulator chunk, the 32 values the
+// lanes of a warp hold (lane = row) with op, transposed: lane l returns the
+// result for column l.  31 shuffles: at each halving step a lane keeps one
+// half of its columns and takes its partner's share of that half.
+template <class Op>
+__device__ __forceinline__ float warp_transpose_reduce(float (&x)[32], Op op) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int h = 16; h >= 1; h >>= 1) {
+    const bool up = (lane & h) != 0;
+#pragma unroll
+    for (int i = 0; i < h; ++i) {
+      const float keep = up ? x[i + h] : x[i];
+      const float send = up ? x[i] : x[i + h];
+      x[i] = op(keep, __shfl_xor_sync(~0u, send, h));
+    }
+  }
+  return x[0];
+}
+
+// Softmax statistics of one 32-row quadrant of a tile for the chunk's
+// hidden states c0 .. c0+31: max of s = logit / T over the quadrant's rows
+// (rows past V_high excluded) and the sum of exp(s - max); lane l writes
+// hidden state c0 + l's pair.  The row kernel folds these into the softmax
+// normaliser and bounds the k-th best score from them.
+__device__ __forceinline__ void quadrant_stats(const TcArgs& a, const float (&r)[32],
+                                               int row, int c0, int quad) {
+  const int lane = threadIdx.x & 31;
+  float sv[32], x[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    sv[j] = row < a.V_high ? __fmul_rn(r[j], a.inv_tau) : -INFINITY;
+    x[j] = sv[j];
+  }
+  const float mx = warp_transpose_reduce(x, [](float p, float q) { return fmaxf(p, q); });
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const float mj = __shfl_sync(~0u, mx, j);
+    x[j] = sv[j] > -INFINITY ? __expf(sv[j] - mj) : 0.f;
+  }
+  const float se = warp_transpose_reduce(x, [](float p, float q) { return p + q; });
+  if (c0 + lane < a.M) a.qstat[(size_t)(c0 + lane) * a.nq + quad] = make_float2(mx, se);
+}
+
 __global__ void __launch_bounds__(kTcThreads, 1)
     head_tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
                         const __grid_constant__ CUtensorMap tmH, TcArgs a) {
@@ -90,10 +147,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = a.stages;
-  const int b_bytes = a.N * kTcBlockK * 2;
-  const int stage_bytes = kTcABytes + b_bytes;
+  const int b_bytes = a.N * kTcBlockK * 2;  // one K atom of H
+  const int A = a.atoms;
+  const int stage_bytes = A * (kTcABytes + b_bytes);
   const int ntiles = (a.V_high + kTcTileRows - 1) / kTcTileRows;
-  const int nkb = (a.d + kTcBlockK - 1) / kTcBlockK;
+  const int natoms = (a.d + kTcBlockK - 1) / kTcBlockK;  // K atoms in all
+  const int nkb = (natoms + A - 1) / A;                   // stages per tile
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -124,7 +183,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 0 && lane == 0 && (int)blockIdx.x < ntiles) {
     tc::prefetch_tensormap(&tmW);
     tc::prefetch_tensormap(&tmH);
-    const int npre = min(nkb, kTcPrefetchKBlocks);
+    const int npre = min(natoms, kTcPrefetchKBlocks);
     for (int kb = 0; kb < npre; ++kb)
       tc::tma_prefetch_l2_2d(&tmW, kb * kTcBlockK, (int)blockIdx.x * kTcTileRows);
   }
@@ -142,10 +201,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             ok = false;
             break;
           }
+          // the stage's K atoms of the W tile are adjacent 128-byte pieces
+          // of the same rows, requested back to back; then H's
           uint8_t* st = smem + (size_t)s * stage_bytes;
-          tc::mbar_arrive_expect_tx(&full[s], (uint32_t)stage_bytes);
-          tc::tma_load_2d(st, &tmW, &full[s], kb * kTcBlockK, tile * kTcTileRows);
-          tc::tma_load_2d(st + kTcABytes, &tmH, &full[s], kb * kTcBlockK, 0);
+          const int na = min(A, natoms - kb * A);
+          tc::mbar_arrive_expect_tx(&full[s], (uint32_t)(na * (kTcABytes + b_bytes)));
+          for (int x = 0; x < na; ++x)
+            tc::tma_load_2d(st + x * kTcABytes, &tmW, &full[s],
+                            (kb * A + x) * kTcBlockK, tile * kTcTileRows);
+          for (int x = 0; x < na; ++x)
+            tc::tma_load_2d(st + A * kTcABytes + x * b_bytes, &tmH, &full[s],
+                            (kb * A + x) * kTcBlockK, 0);
           ++issued;
           if (++s == S) { s = 0; ph ^= 1u; }
         }
@@ -177,12 +243,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (!wait_or_abort(&full[s], ph, &abort_flag)) { ok = false; break; }
           tc::tc_fence_after();
           const uint32_t a_base = tc::smem_u32(smem + (size_t)s * stage_bytes);
-          const uint32_t b_base = a_base + kTcABytes;
+          const uint32_t b_base = a_base + A * kTcABytes;
+          const int na = min(A, natoms - kb * A);
+          for (int x = 0; x < na; ++x)
 #pragma unroll
-          for (int j = 0; j < kTcBlockK / 16; ++j)
-            tc::mma_bf16(d_tmem, tc::sdesc_k_sw128(a_base + 32 * j),
-                         tc::sdesc_k_sw128(b_base + 32 * j), idesc,
-                         (kb > 0 || j > 0) ? 1u : 0u);
+            for (int j = 0; j < kTcBlockK / 16; ++j)
+              tc::mma_bf16(d_tmem,
+                           tc::sdesc_k_sw128(a_base + x * kTcABytes + 32 * j),
+                           tc::sdesc_k_sw128(b_base + x * b_bytes + 32 * j), idesc,
+                           (kb > 0 || x > 0 || j > 0) ? 1u : 0u);
           tc::mma_commit(&empty[s]);  // stage reusable once these complete
           if (++s == S) { s = 0; ph ^= 1u; }
         }
@@ -208,18 +277,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       tc::tc_fence_after();
       const int row = tile * kTcTileRows + 32 * q + lane;
+      const float b = row < a.V_high && a.bias ? __ldg(a.bias + row) : 0.f;
       for (int c0 = 0; c0 < a.N; c0 += 32) {
         float r[32];
         tc::tmem_ld_32x32(tmem + ((uint32_t)(32 * q) << 16) +
                               (uint32_t)(acc * a.NB + c0),
                           r);
         tc::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] += b;
         if (row < a.V_high) {
-          const float b = a.bias ? __ldg(a.bias + row) : 0.f;
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            if (c0 + j < a.M) a.logits[(size_t)(c0 + j) * a.V_high + row] = r[j] + b;
+            if (c0 + j < a.M) a.logits[(size_t)(c0 + j) * a.V_high + row] = r[j];
         }
+        if (a.qstat) quadrant_stats(a, r, row, c0, tile * 4 + q);
       }
       tc::tc_fence_before();
       __syncwarp();
@@ -443,6 +515,237 @@ __global__ void __launch_bounds__(kRowThreads, 4)
   if (tid == 0) a.tickets[m] = 0u;
 }
 
+// ------------------------------------------- per-row top-k from statistics
+// Top-k calls (no sampling).  One CTA per hidden state m, after the GEMM:
+//   * folds the quadrant statistics into the softmax normaliser:
+//     Mg = max_q max_q,  Sg = sum_q sum_q * exp(max_q - Mg);
+//   * bounds the k-th best score from below: quadrants are dealt into 32
+//     disjoint groups by index mod 32 (every group holds some once there
+//     are 32 quadrants); the k-th largest of the group maxima is the score
+//     of one of k different logits, so it is at most the k-th best score, L;
+//   * a logit with s >= L lies in a quadrant whose maximum is >= L: only
+//     those quadrants (a few dozen on real data) are read, 32 logits each,
+//     and the keys (s, full id) with s >= L are kept in shared memory,
+//     ranked by counting, and the k best written as ids and
+//     exp(s - Mg) / Sg.
+// If more than kSelQuads quadrants reach L, the whole row is scanned
+// instead.  If more than kSelCap keys reach L (scores tied at the top), the exact
+// k-th best key is found instead by an 8-bit radix select over the 64-bit
+// keys (keys are distinct: the full id breaks ties), then the k keys at or
+// above it are ranked.
+constexpr int kSelThreads = 1024;
+constexpr int kSelWarps = kSelThreads / 32;  // >= kTopKMax groups
+constexpr int kSelCap = 2048;
+constexpr int kSelBatch = 8;  // float4 of logits per thread per batch (row scan)
+constexpr int kSelQuads = 256;  // quadrants read directly
+constexpr int kSelQPer = 4;     // quadrant statistics per thread in registers
+
+struct SelArgs {
+  const float* logits;  // [M][V_high], bias added
+  const float2* qstat;  // [M][nq]
+  int nq, V_high, k;
+  const int32_t* t2f;
+  int32_t* out_ids;
+  float* out_probs;
+  float inv_tau;
+};
+
+__global__ void __launch_bounds__(kSelThreads, 1)
+    rows_select_kernel(SelArgs a) {
+  __shared__ float red[kSelWarps];
+  __shared__ unsigned wkey[32];  // float_key of each group's maximum (0: empty)
+  __shared__ entry_key surv[kSelCap];
+  __shared__ float surv_s[kSelCap];
+  __shared__ unsigned hist[256];
+  __shared__ int cquad[kSelQuads];
+  __shared__ int s_cnt, s_need, s_digit, s_nq;
+  __shared__ unsigned s_lkey;
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int m = blockIdx.x, k = a.k;
+  const float2* qs = a.qstat + (size_t)m * a.nq;
+  const float* row = a.logits + (size_t)m * a.V_high;
+  const bool vec = ((a.V_high & 3) == 0) &&
+                   ((reinterpret_cast<uintptr_t>(a.logits) & 15) == 0);
+
+
+  // the first kSelQPer * kSelThreads quadrants' statistics stay in
+  // registers (one L2 round trip); any beyond are read again per pass
+  float2 st[kSelQPer];
+#pragma unroll
+  for (int r = 0; r < kSelQPer; ++r) {
+    const int q = tid + r * kSelThreads;
+    st[r] = q < a.nq ? __ldcg(&qs[q]) : make_float2(-INFINITY, 0.f);
+  }
+  auto stat = [&](int q, int r) { return r < kSelQPer ? st[r] : __ldcg(&qs[q]); };
+  if (tid < 32) wkey[tid] = 0u;
+  if (tid == 0) { s_cnt = 0; s_nq = 0; }
+  __syncthreads();
+  float lm = -INFINITY;
+  unsigned gk = 0u;  // this thread's largest quadrant maximum (0: none)
+#pragma unroll 1
+  for (int q = tid, r = 0; q < a.nq; q += kSelThreads, ++r) {
+    const float mq = stat(q, r).x;
+    lm = fmaxf(lm, mq);
+    if (mq > -INFINITY) gk = max(gk, float_key(mq));
+  }
+  // thread t holds quadrants t + 1024 j, all = t mod 32 = its lane
+  if (gk) atomicMax(&wkey[lane], gk);
+  const float mg = block_max<kSelThreads>(lm, red);  // (its barriers publish wkey)
+  float ls = 0.f;
+#pragma unroll 1
+  for (int q = tid, r = 0; q < a.nq; q += kSelThreads, ++r) {
+    const float2 sq = stat(q, r);
+    if (sq.y > 0.f) ls += sq.y * __expf(sq.x - mg);
+  }
+  if (warp == 0) {
+    // L: the k-th largest group maximum (ties by group index); an empty
+    // group (key 0) among the k best makes L = 0, which keeps every key
+    const unsigned v = wkey[lane];
+    int rank = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const unsigned u = __shfl_sync(~0u, v, j);
+      rank += (u > v) || (u == v && j < lane);
+    }
+    if (rank == k - 1) s_lkey = v;
+  }
+  const float sg = block_sum<kSelThreads>(ls, red);  // (its barriers publish s_lkey)
+  const unsigned lkey = s_lkey;
+  // the quadrants whose maximum reaches L
+#pragma unroll 1
+  for (int q = tid, r = 0; q < a.nq; q += kSelThreads, ++r) {
+    const float mq = stat(q, r).x;
+    if (mq > -INFINITY && float_key(mq) >= lkey) {
+      const int p = atomicAdd(&s_nq, 1);
+      if (p < kSelQuads) cquad[p] = q;
+    }
+  }
+  __syncthreads();
+  const int nquad = s_nq;
+
+  auto score = [&](int i) { return __fmul_rn(__ldcg(row + i), a.inv_tau); };
+  auto fid = [&](int i) { return a.t2f ? __ldg(a.t2f + i) : i; };
+  auto keep_id = [&](int f, float sv) {
+    const int p = atomicAdd(&s_cnt, 1);
+    if (p < kSelCap) {
+      surv[p] = make_key(sv, f);
+      surv_s[p] = sv;
+    }
+  };
+  auto keep = [&](int i, float sv) { keep_id(fid(i), sv); };
+  if (nquad <= kSelQuads) {
+    // logit and full id loaded together: one round trip
+    for (int j = tid; j < nquad * 32; j += kSelThreads) {
+      const int i = cquad[j >> 5] * 32 + (j & 31);
+      if (i < a.V_high) {
+        const float l = __ldcg(row + i);
+        const int f = fid(i);
+        const float sv = __fmul_rn(l, a.inv_tau);
+        if (float_key(sv) >= lkey) keep_id(f, sv);
+      }
+    }
+  } else if (vec) {
+    float4 x[kSelBatch];
+    for (int i0 = 4 * tid; i0 < a.V_high; i0 += 4 * kSelThreads * kSelBatch) {
+#pragma unroll
+      for (int b = 0; b < kSelBatch; ++b) {
+        const int i = i0 + 4 * kSelThreads * b;
+        x[b] = i < a.V_high ? __ldcg(reinterpret_cast<const float4*>(row + i))
+                            : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      }
+#pragma unroll
+      for (int b = 0; b < kSelBatch; ++b) {
+        const int i = i0 + 4 * kSelThreads * b;
+        const float v[4] = {__fmul_rn(x[b].x, a.inv_tau), __fmul_rn(x[b].y, a.inv_tau),
+                            __fmul_rn(x[b].z, a.inv_tau), __fmul_rn(x[b].w, a.inv_tau)};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (i < a.V_high && float_key(v[e]) >= lkey) keep(i + e, v[e]);
+      }
+    }
+  } else {
+    for (int i = tid; i < a.V_high; i += kSelThreads) {
+      const float sv = score(i);
+      if (float_key(sv) >= lkey) keep(i, sv);
+    }
+  }
+  __syncthreads();
+  int S = s_cnt;
+
+  if (S > kSelCap) {
+    // radix select of the k-th best key among those reaching L, most
+    // significant digit first
+    entry_key prefix = 0ull, pmask = 0ull;
+    int need = k;
+    for (int p = 7; p >= 0; --p) {
+      if (tid < 256) hist[tid] = 0u;
+      __syncthreads();
+      for (int i = tid; i < a.V_high; i += kSelThreads) {
+        const float sv = score(i);
+        if (float_key(sv) < lkey) continue;
+        const entry_key key = make_key(sv, fid(i));
+        if ((key & pmask) == prefix) atomicAdd(&hist[(unsigned)(key >> (8 * p)) & 255u], 1u);
+      }
+      __syncthreads();
+      if (warp == 0) {
+        // lane l holds digits 255-8l .. 248-8l; find the digit where the
+        // count of larger-or-equal digits first reaches need
+        unsigned c[8], tot = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) { c[e] = hist[255 - 8 * lane - e]; tot += c[e]; }
+        unsigned before = tot;  // inclusive scan over lanes, then exclusive
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const unsigned y = __shfl_up_sync(~0u, before, o);
+          if (lane >= o) before += y;
+        }
+        before -= tot;
+        if (before < (unsigned)need && before + tot >= (unsigned)need) {
+          unsigned run = before;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            if (run + c[e] >= (unsigned)need) {
+              s_digit = 255 - 8 * lane - e;
+              s_need = need - (int)run;
+              break;
+            }
+            run += c[e];
+          }
+        }
+      }
+      __syncthreads();
+      prefix |= (entry_key)(unsigned)s_digit << (8 * p);
+      pmask |= 0xffull << (8 * p);
+      need = s_need;
+      __syncthreads();
+    }
+    // prefix is the k-th best key: collect the k keys at or above it
+    if (tid == 0) s_cnt = 0;
+    __syncthreads();
+    for (int i = tid; i < a.V_high; i += kSelThreads) {
+      const float sv = score(i);
+      if (float_key(sv) < lkey) continue;
+      if (make_key(sv, fid(i)) >= prefix) keep(i, sv);
+    }
+    __syncthreads();
+    S = min(s_cnt, k);
+  }
+
+  int32_t* ids = a.out_ids + (size_t)m * k;
+  float* probs = a.out_probs + (size_t)m * k;
+  for (int c = tid; c < S; c += kSelThreads) {
+    const entry_key xk = surv[c];
+    int rank = 0;
+    for (int q = 0; q < S; ++q) rank += surv[q] > xk;
+    if (rank < k) {
+      ids[rank] = key_id(xk);
+      probs[rank] = expf(surv_s[c] - mg) / sg;
+    }
+  }
+}
+
 // ------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   static std::once_flag once;
@@ -480,15 +783,17 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
 // 128, per-row tickets from byte 1024), then per-row partials of the top-k
 // kernel, then the fp32 logits.
 struct TcLayout {
-  size_t tickets, part, logits, total;
+  size_t tickets, part, qstat, logits, total;
 };
 static size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 static int row_parts(int V_high) { return (V_high + kRowSpan - 1) / kRowSpan; }
+static int quadrants(int V_high) { return 4 * ((V_high + kTcTileRows - 1) / kTcTileRows); }
 static TcLayout tc_layout(int M, int V_high, int k) {
   TcLayout L;
   L.tickets = kHeadRowTicketOffset;
   L.part = kHeadTicketBytes;
-  L.logits = L.part + round256((size_t)M * row_parts(V_high) * (2 + 3 * k) * 4);
+  L.qstat = L.part + round256((size_t)M * row_parts(V_high) * (2 + 3 * k) * 4);
+  L.logits = L.qstat + round256((size_t)M * quadrants(V_high) * sizeof(float2));
   L.total = L.logits + (size_t)M * V_high * 4;
   return L;
 }
@@ -519,8 +824,20 @@ vt_status head_tc(const uint16_t* H, int M, int d, int64_t ldh,
   a.logits = logits;
   a.bias = opt.bias;
   a.err = err;
-  const int stage_bytes = kTcABytes + a.N * kTcBlockK * 2;
-  a.stages = std::min<int>(kTcMaxStages, (di.max_smem_optin - 4096) / stage_bytes);
+  // top-k calls: quadrant statistics for rows_select_kernel; sampling calls
+  // score every logit with its noise in rows_topk_kernel instead
+  const bool stats = !opt.sample;
+  a.qstat = stats ? reinterpret_cast<float2*>(wsb + L.qstat) : nullptr;
+  a.nq = quadrants(V_high);
+  a.inv_tau = 1.0f / opt.tau;
+  // K atoms per stage: the widest (up to kTcMaxAtoms) that still leaves
+  // kTcMinStages stages in shared memory.
+  const int atom_bytes = kTcABytes + a.N * kTcBlockK * 2;
+  const int fit = (di.max_smem_optin - 4096) / atom_bytes;  // atoms that fit
+  a.atoms = 1;
+  while (a.atoms * 2 <= kTcMaxAtoms && fit / (a.atoms * 2) >= kTcMinStages) a.atoms *= 2;
+  const int stage_bytes = a.atoms * atom_bytes;
+  a.stages = std::min<int>(kTcMaxStages, fit / a.atoms);
   if (a.stages < 2) return fail(VT_ERR_UNSUPPORTED, "head_tc: stages do not fit");
   CUtensorMap tmW, tmH;
   if (!make_map(&tmW, W, (uint64_t)V_high, (uint64_t)d, (uint64_t)d, kTcTileRows) ||
@@ -537,6 +854,24 @@ vt_status head_tc(const uint16_t* H, int M, int d, int64_t ldh,
     return fail(VT_ERR_CUDA, std::string("head_tc_gemm_kernel: ") + cudaGetErrorString(e));
   vt_status st = launch_status("head_tc_gemm_kernel");
   if (st != VT_OK) return st;
+  if (stats) {
+    SelArgs sa;
+    sa.logits = logits;
+    sa.qstat = a.qstat;
+    sa.nq = a.nq;
+    sa.V_high = V_high;
+    sa.k = k;
+    sa.t2f = t2f;
+    sa.out_ids = out_ids;
+    sa.out_probs = out_probs;
+    sa.inv_tau = a.inv_tau;
+    // a programmatic dependent of the GEMM, like the per-row kernel below
+    const cudaError_t e3 = launch_dependent(rows_select_kernel, dim3(M),
+                                            dim3(kSelThreads), 0, s, sa);
+    if (e3 != cudaSuccess)
+      return fail(VT_ERR_CUDA, std::string("rows_select_kernel: ") + cudaGetErrorString(e3));
+    return launch_status("rows_select_kernel");
+  }
   const int P = row_parts(V_high);
   if (P * k > kRowSurvivors)
     return fail(VT_ERR_UNSUPPORTED, "head_tc: V_high * k too large for the row merge");

@@ -147,3 +147,30 @@ def test_tc_row_survivor_worst_case_k32():
     ref = oracle.draft_head(bits_host(Hd), bits_host(Wd), t2f.cpu().numpy(), k)
     assert np.array_equal(ids.cpu().numpy(), ref["ids"])
     np.testing.assert_allclose(probs.cpu().numpy(), ref["probs"], atol=1e-6)
+
+
+@pytest.mark.parametrize("V_high", [32768, 32771])
+def test_tc_all_quadrants_reach_the_bound(V_high):
+    """Every 32-row quadrant holds one logit of exactly 2.0 and the rest
+    below: the bound on the k-th best score equals 2.0, every quadrant
+    reaches it (more than can be read one by one), so the row is scanned
+    whole; the 2.0 entries tie and the k with the lowest full ids win, as in
+    the oracle (logits exact: one-hot hidden states)."""
+    dev = need_cuda()
+    d, M, k = 64, 2, 10
+    rng = np.random.default_rng(V_high)
+    vals = 1.0 + rng.integers(0, 64, V_high) / 128.0  # bf16-exact, < 2
+    top = np.arange(0, V_high, 32) + rng.integers(0, 32, (V_high + 31) // 32)
+    vals[top[top < V_high]] = 2.0
+    W = np.zeros((V_high, d), np.float32)
+    W[:, 0] = vals
+    Hn = np.zeros((M, d), np.float32)
+    Hn[:, 0] = 1.0
+    Wd = torch.from_numpy(W).to(torch.bfloat16).to(dev)
+    Hd = torch.from_numpy(Hn).to(torch.bfloat16).to(dev)
+    t2f = synth.rank_permutation(2 * V_high, 92)[:V_high].to(dev)
+    ids, probs = vt.draft_head(Hd, Wd, t2f, k)
+    torch.cuda.synchronize()
+    ref = oracle.draft_head(bits_host(Hd), bits_host(Wd), t2f.cpu().numpy(), k)
+    assert np.array_equal(ids.cpu().numpy(), ref["ids"])
+    np.testing.assert_allclose(probs.cpu().numpy(), ref["probs"], atol=1e-6)
