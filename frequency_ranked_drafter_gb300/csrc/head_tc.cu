@@ -50,8 +50,9 @@ constexpr int kTcPrefetchKBlocks = 32;
 constexpr int kTcBlockK = 64;  // bf16 per K atom: 128 bytes, one swizzle row
 // A stage holds up to kTcMaxAtoms K atoms (adjacent 128-byte pieces of the
 // same 128 W_high rows, loaded back to back), as many as leave kTcMinStages
-// stages: wider stages give DRAM longer runs per row (M = 60, V_high =
-// 32768: 68.5 us with one atom a stage, 59.2 us with two).
+// stages: wider stages keep more of W_high in flight per SM (M = 60,
+// V_high = 32768: 68.5 us with one atom a stage, 59.2 us with two, 53.0
+// with three).
 constexpr int kTcMaxAtoms = 4;
 constexpr int kTcMinStages = 3;
 constexpr int kTcTileRows = 128;
@@ -834,8 +835,7 @@ vt_status head_tc(const uint16_t* H, int M, int d, int64_t ldh,
   // kTcMinStages stages in shared memory.
   const int atom_bytes = kTcABytes + a.N * kTcBlockK * 2;
   const int fit = (di.max_smem_optin - 4096) / atom_bytes;  // atoms that fit
-  a.atoms = 1;
-  while (a.atoms * 2 <= kTcMaxAtoms && fit / (a.atoms * 2) >= kTcMinStages) a.atoms *= 2;
+  a.atoms = std::max(1, std::min(kTcMaxAtoms, fit / kTcMinStages));
   const int stage_bytes = a.atoms * atom_bytes;
   a.stages = std::min<int>(kTcMaxStages, fit / a.atoms);
   if (a.stages < 2) return fail(VT_ERR_UNSUPPORTED, "head_tc: stages do not fit");
