@@ -177,6 +177,26 @@ __global__ void __launch_bounds__(kRowQThreads, 1)
   __shared__ float2 st_all;
   const int m = blockIdx.y;
   const float* row = logits + (size_t)m * V_high;
+  const int f_begin = blockIdx.x * span, f_end = min(V, f_begin + span);
+  // this thread's f2t entries of the fill: the first step's are requested
+  // before the row is staged, each next step's before the current one is
+  // written (two steps of 16-byte loads in flight)
+  auto load_idx = [&](int f0, int (&idx)[kFillIds]) {
+    if (vec && f2t && f0 + kFillIds <= f_end) {
+      const int4 a = __ldg(reinterpret_cast<const int4*>(f2t + f0));
+      const int4 b = __ldg(reinterpret_cast<const int4*>(f2t + f0) + 1);
+      idx[0] = a.x; idx[1] = a.y; idx[2] = a.z; idx[3] = a.w;
+      idx[4] = b.x; idx[5] = b.y; idx[6] = b.z; idx[7] = b.w;
+    } else {
+#pragma unroll
+      for (int j = 0; j < kFillIds; ++j)
+        idx[j] = f0 + j < f_end ? (f2t ? __ldg(f2t + f0 + j) : f0 + j) : -1;
+    }
+  };
+  constexpr int kStep = kRowQThreads * kFillIds;
+  int idx[kFillIds];
+  int f0 = f_begin + threadIdx.x * kFillIds;
+  if (f0 < f_end) load_idx(f0, idx);
   float mm = -INFINITY, ss = 0.f;
   auto add = [&](float x) {
     if (x > mm) {
@@ -239,21 +259,10 @@ __global__ void __launch_bounds__(kRowQThreads, 1)
   __syncthreads();
   const float mx = st_all.x, inv_sum = st_all.y;
   float* qm = q + (size_t)m * V;
-  const int f_begin = blockIdx.x * span, f_end = min(V, f_begin + span);
-  for (int f0 = f_begin + threadIdx.x * kFillIds; f0 < f_end;
-       f0 += kRowQThreads * kFillIds) {
-    int idx[kFillIds];
+  for (; f0 < f_end; f0 += kStep) {
+    int nidx[kFillIds];
+    if (f0 + kStep < f_end) load_idx(f0 + kStep, nidx);
     const bool full = vec && f0 + kFillIds <= f_end;
-    if (full && f2t) {
-      const int4 a = __ldg(reinterpret_cast<const int4*>(f2t + f0));
-      const int4 b = __ldg(reinterpret_cast<const int4*>(f2t + f0) + 1);
-      idx[0] = a.x; idx[1] = a.y; idx[2] = a.z; idx[3] = a.w;
-      idx[4] = b.x; idx[5] = b.y; idx[6] = b.z; idx[7] = b.w;
-    } else {
-#pragma unroll
-      for (int j = 0; j < kFillIds; ++j)
-        idx[j] = f0 + j < f_end ? (f2t ? __ldg(f2t + f0 + j) : f0 + j) : -1;
-    }
     float o[kFillIds];
 #pragma unroll
     for (int j = 0; j < kFillIds; ++j)
@@ -267,6 +276,8 @@ __global__ void __launch_bounds__(kRowQThreads, 1)
       for (int j = 0; j < kFillIds; ++j)
         if (f0 + j < f_end) qm[f0 + j] = o[j];
     }
+#pragma unroll
+    for (int j = 0; j < kFillIds; ++j) idx[j] = nidx[j];
   }
 }
 
