@@ -433,8 +433,9 @@ def draft_head_host(H_host: torch.Tensor, W_high: torch.Tensor,
 class HostDraftHead:
     """Draft steps from host memory through the library's host step
     (vt_host_step_*): each call copies the hidden states into the handle's
-    pinned staging buffer, launches one CUDA graph (copy in, the head, one
-    copy of ids and probabilities back), synchronises, and returns host
+    pinned staging buffer, launches one CUDA graph (copy in, then the head,
+    whose kernel writes ids and probabilities into pinned host memory),
+    synchronises, and returns host
     tensors (ids [M, k] int32, probs [M, k] float32) that the next call
     overwrites.  ``W_high``, ``t2f``, ``k``, M and the options (bias,
     temperature) are fixed; drawing is not offered (a replayed graph repeats

@@ -5,10 +5,15 @@
 // a different process's buffers) pays per step for: the copy of the step's
 // hidden states to the device, the head, the copy of ids and probabilities
 // back, and a synchronise.  The handle captures the three device operations
-// once (device copy of H from a pinned staging buffer, vt_draft_head_ex, one
-// device-to-host copy of ids and probabilities packed together) into a CUDA
-// graph on its own stream; each step is then a host copy of H into the
-// staging buffer, one graph launch, one synchronise and a host copy out.
+// once into a CUDA graph on its own stream: a small kernel copies H from a
+// pinned staging buffer to the device and lets the head start at once (the
+// head is a programmatic dependent: it prefetches its first weight rows
+// while H crosses, and waits for the copy before reading it), then
+// vt_draft_head_ex, whose last CTA writes ids and probabilities straight into
+// a pinned host buffer (pinned memory is addressable from the device, so no
+// copy node follows).  Each step is then a host copy of H into the staging
+// buffer, one graph launch, one synchronise (which also makes the kernel's
+// host writes visible) and a host copy out.
 // The pages have no counterpart: it serves the end-to-end use of the head.
 #include <cstring>
 #include <new>
@@ -20,13 +25,26 @@ struct vt_host_step {
   cudaStream_t stream = nullptr;
   cudaGraphExec_t exec = nullptr;
   uint16_t* H_pinned = nullptr;   // host, pinned [M, d]
-  int32_t* out_pinned = nullptr;  // host, pinned [2, M, k] (ids, prob bits)
+  int32_t* out_pinned = nullptr;  // host, pinned [2, M, k] (ids, prob bits),
+                                  // written by the head's kernel
   uint16_t* H_dev = nullptr;      // device [M, d]
-  int32_t* out_dev = nullptr;     // device [2, M, k]
   void* ws = nullptr;             // device head workspace
 };
 
 namespace {
+
+constexpr int kCopyThreads = 256;
+
+// dst[i] = src[i] for n 16-byte words, src in pinned host memory.  Triggers
+// its dependents first, so the head's grid can become resident meanwhile.
+__global__ void __launch_bounds__(kCopyThreads)
+    host_h_copy_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                       int n) {
+  vt::grid_launch_dependents();
+  for (int i = blockIdx.x * kCopyThreads + threadIdx.x; i < n;
+       i += gridDim.x * kCopyThreads)
+    dst[i] = src[i];
+}
 
 void destroy(vt_host_step* h) {
   if (!h) return;
@@ -35,7 +53,6 @@ void destroy(vt_host_step* h) {
   if (h->H_pinned) cudaFreeHost(h->H_pinned);
   if (h->out_pinned) cudaFreeHost(h->out_pinned);
   if (h->H_dev) cudaFree(h->H_dev);
-  if (h->out_dev) cudaFree(h->out_dev);
   if (h->ws) cudaFree(h->ws);
   delete h;
 }
@@ -75,21 +92,30 @@ extern "C" vt_status vt_host_step_create(const uint16_t* W_high, int32_t V_high,
   if (cudaMallocHost(&h->H_pinned, hbytes) != cudaSuccess ||
       cudaMallocHost(&h->out_pinned, obytes) != cudaSuccess ||
       cudaMalloc(&h->H_dev, hbytes) != cudaSuccess ||
-      cudaMalloc(&h->out_dev, obytes) != cudaSuccess ||
       cudaMalloc(&h->ws, wbytes) != cudaSuccess)
     return bad("allocation");
   std::memset(h->H_pinned, 0, hbytes);
   if (cudaMemsetAsync(h->ws, 0, wbytes, h->stream) != cudaSuccess) return bad("memset");
-  int32_t* ids_dev = h->out_dev;
-  float* probs_dev = reinterpret_cast<float*>(h->out_dev + (size_t)M * k);
+  // the device address of the pinned output buffer (the same pointer under
+  // unified addressing)
+  int32_t* out_devp = nullptr;
+  if (cudaHostGetDevicePointer((void**)&out_devp, h->out_pinned, 0) != cudaSuccess)
+    return bad("output buffer mapping");
+  int32_t* ids_dev = out_devp;
+  float* probs_dev = reinterpret_cast<float*>(out_devp + (size_t)M * k);
+  uint16_t* H_src = nullptr;
+  if (cudaHostGetDevicePointer((void**)&H_src, h->H_pinned, 0) != cudaSuccess)
+    return bad("staging buffer mapping");
+  const int n16 = (int)(hbytes / 16);  // d % 8 == 0: whole 16-byte words
+  const int copy_blocks = std::min(64, (n16 + kCopyThreads - 1) / kCopyThreads);
   // one eager step first (kernel attributes, first-call set-up), then capture
   for (int pass = 0; pass < 2; ++pass) {
     if (pass == 1 &&
         cudaStreamBeginCapture(h->stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
       return bad("begin capture");
-    if (cudaMemcpyAsync(h->H_dev, h->H_pinned, hbytes, cudaMemcpyHostToDevice,
-                        h->stream) != cudaSuccess)
-      return bad("copy in");
+    host_h_copy_kernel<<<copy_blocks, kCopyThreads, 0, h->stream>>>(
+        reinterpret_cast<const uint4*>(H_src), reinterpret_cast<uint4*>(h->H_dev), n16);
+    if (cudaGetLastError() != cudaSuccess) return bad("copy in");
     const vt_status st = vt_draft_head_ex(h->H_dev, M, d, d, W_high, V_high, t2f, k,
                                           opts, ids_dev, probs_dev, nullptr, h->ws,
                                           wbytes, h->stream);
@@ -102,9 +128,6 @@ extern "C" vt_status vt_host_step_create(const uint16_t* W_high, int32_t V_high,
       destroy(h);
       return st;
     }
-    if (cudaMemcpyAsync(h->out_pinned, h->out_dev, obytes, cudaMemcpyDeviceToHost,
-                        h->stream) != cudaSuccess)
-      return bad("copy out");
     if (pass == 0 && cudaStreamSynchronize(h->stream) != cudaSuccess)
       return bad("first step");
   }

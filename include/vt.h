@@ -322,8 +322,9 @@ vt_status vt_draft_q(const float* logits, int32_t M, int32_t V_high,
  * The pages have no counterpart; this serves callers whose hidden states
  * live on the host.  The handle owns a stream, pinned staging buffers,
  * device buffers, a zero-filled head workspace and a CUDA graph of: copy of
- * the staged H [M, d] to the device, vt_draft_head_ex, one copy of the ids
- * and probabilities back.
+ * the staged H [M, d] to the device, then vt_draft_head_ex writing the ids
+ * and probabilities straight into a pinned host buffer (device-addressable;
+ * no copy node follows).
  *
  *   vt_host_step_create: W_high, V_high, d, t2f, M (1..256), k and opts are
  *     fixed for the handle's life (W_high and t2f must stay valid); opts may
