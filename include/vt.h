@@ -177,6 +177,11 @@ vt_status vt_gather_bias(const float* b, int64_t V, const int32_t* t2f,
  * Paths: M = 1 runs a split-V GEMV (CUDA cores, one launch); M >= 2 runs a
  * tcgen05 tensor-core GEMM over all M rows at once plus a per-row softmax
  * and top-k kernel.  One workspace can serve calls of any M.
+ * The head's kernels are launched as programmatic dependents of the work
+ * ahead of them in the stream: they may become resident while the previous
+ * kernel finishes and ask L2 for their first W_high rows meanwhile (a
+ * prefetch hint), but read H, t2f, the bias and the workspace, and write
+ * anything, only after that kernel has completed; stream order is kept.
  * ------------------------------------------------------------------------ */
 size_t vt_draft_head_workspace_size(int32_t M, int32_t V_high, int32_t k);
 vt_status vt_draft_head(const uint16_t* H, int32_t M, int32_t d, int64_t ldh,
