@@ -85,6 +85,7 @@ def load(build_if_missing: bool = True):
             "vt_draft_head_ex": ([p, i32, i32, i64, p, i32, p, i32,
                                   ctypes.POINTER(HeadOptions), p, p, p, p, sz,
                                   p], ctypes.c_int),
+            "vt_selftest_wait_timeout": ([p, i64, p], ctypes.c_int),
             "vt_draft_noise": ([ctypes.c_uint64, ctypes.c_uint64, i32, p, i64,
                                 p, p], ctypes.c_int),
             "vt_draft_q_workspace_size": ([i32], sz),

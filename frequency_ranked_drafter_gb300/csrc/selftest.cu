@@ -1,0 +1,43 @@
+// vt_selftest_wait_timeout — makes the library's bounded device wait run
+// out, so that a caller (or a test) can see the failure path work: the
+// kernel sets the error word and returns, and the context stays usable.
+//
+// Every wait of the library's kernels on an mbarrier (TMA stages, MMA
+// completion, the accumulator hand-over, the final merge's bulk copy) is
+// tc::mbar_wait with a cycle budget; on expiry the kernel records
+// VT_ERR_TIMEOUT in the workspace error word and stops.  Here one CTA
+// initialises an mbarrier on which nothing ever arrives and waits on it with
+// the caller's budget.  The pages have no counterpart.
+#include "head_common.cuh"
+
+namespace vt {
+namespace {
+
+__global__ void __launch_bounds__(32)
+    wait_timeout_kernel(unsigned* err, long long budget) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    tc::mbar_init(&bar, 1);
+    tc::fence_barrier_init();
+  }
+  __syncwarp();
+  // nothing arrives on `bar`: the wait gives up after `budget` cycles
+  if (threadIdx.x == 0 && !tc::mbar_wait(&bar, 0u, budget))
+    atomicExch(err, (unsigned)VT_ERR_TIMEOUT);
+}
+
+}  // namespace
+}  // namespace vt
+
+extern "C" vt_status vt_selftest_wait_timeout(uint32_t* err_word,
+                                              int64_t budget_cycles,
+                                              void* stream) {
+  using namespace vt;
+  if (!err_word || !aligned(err_word, 4))
+    return fail(VT_ERR_INVALID_ARG, "vt_selftest_wait_timeout: null or misaligned error word");
+  if (budget_cycles < 1 || budget_cycles > (int64_t(1) << 31))
+    return fail(VT_ERR_INVALID_ARG,
+                "vt_selftest_wait_timeout: budget must be 1 .. 2^31 cycles");
+  wait_timeout_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(err_word, (long long)budget_cycles);
+  return launch_status("wait_timeout_kernel");
+}

@@ -323,6 +323,24 @@ vt_status vt_draft_q(const float* logits, int32_t M, int32_t V_high,
                      float* q, void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * vt_selftest_wait_timeout — runs the library's bounded device wait until it
+ * gives up, to check the failure path.  The pages have no counterpart.
+ *
+ * Every wait of the library's kernels on an mbarrier is bounded by a cycle
+ * budget (about a second); when it runs out the kernel writes
+ * VT_ERR_TIMEOUT to its error word (byte 128 of the head workspace), stops
+ * issuing work and returns, and the context stays usable.  This call
+ * launches one 32-thread CTA that waits on an mbarrier nothing arrives on,
+ * with the given budget, then writes VT_ERR_TIMEOUT to *err_word.
+ *
+ *   err_word      (device) uint32, 4-byte aligned; set to VT_ERR_TIMEOUT.
+ *   budget_cycles 1 .. 2^31 SM clock cycles (2e6 is about a millisecond).
+ * Argument errors return VT_ERR_INVALID_ARG with nothing launched.
+ * ------------------------------------------------------------------------ */
+vt_status vt_selftest_wait_timeout(uint32_t* err_word, int64_t budget_cycles,
+                                   void* stream);
+
+/* ------------------------------------------------------------------------
  * vt_host_step_* — draft steps from host memory, each one CUDA-graph launch.
  * The pages have no counterpart; this serves callers whose hidden states
  * live on the host.  The handle owns a stream, pinned staging buffers,

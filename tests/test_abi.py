@@ -211,3 +211,13 @@ def test_host_step_rejects_bad_arguments(lib):
     assert not h.value
     assert lib.vt_host_step_run(None, FAKE, FAKE, FAKE) == INVALID
     lib.vt_host_step_destroy(None)
+
+
+def test_selftest_wait_timeout_rejects_bad_arguments(lib):
+    """Checked on the host, nothing launched: no error word, a misaligned
+    one, and budgets outside 1 .. 2^31 cycles."""
+    assert lib.vt_selftest_wait_timeout(None, 1000, None) == INVALID
+    assert lib.vt_selftest_wait_timeout(FAKE + 2, 1000, None) == INVALID
+    assert lib.vt_selftest_wait_timeout(FAKE, 0, None) == INVALID
+    assert lib.vt_selftest_wait_timeout(FAKE, (1 << 31) + 1, None) == INVALID
+    assert b"budget" in lib.vt_last_error()
