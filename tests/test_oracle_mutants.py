@@ -52,6 +52,8 @@ OPTION_MUTANTS = {
     "philox_swapped_halves": ("c[1] = lo1;", "c[1] = lo0;"),
     "noise_by_trimmed_index": ("gumbel_noise(seed, offset, m_base + m, full_id(i))",
                                "gumbel_noise(seed, offset, m_base + m, i)"),
+    "noise_row_ignores_m_base": ("gumbel_noise(seed, offset, m_base + m, full_id(i))",
+                                 "gumbel_noise(seed, offset, m, full_id(i))"),
     "noise_ignores_row": ("static_cast<uint32_t>(full_id), static_cast<uint32_t>(m),",
                           "static_cast<uint32_t>(full_id), 0u,"),
     "noise_ignores_offset_high": ("static_cast<uint32_t>(offset >> 32)};",

@@ -167,6 +167,43 @@ def test_trimmed_draw_equals_untrimmed_draw_when_kept(oracle_lib):
     assert np.array_equal(full["ids"][kept, 0], trim["ids"][kept, 0])
 
 
+def philox_gumbel(seed, offset, m, full_id):
+    """Gumbel noise of one token built from the generator's block alone
+    (the block is pinned by the published known-answer vectors): counter
+    (full id, hidden state, offset low word, offset high word), key (seed
+    low word, seed high word); u from the top 23 bits of word 0 at the
+    middle of its cell; g = -log(-log(u))."""
+    x = oracle.philox4x32_10(
+        (full_id, m, offset & MASK, offset >> 32), (seed & MASK, seed >> 32))[0]
+    u = ((int(x) >> 9) + 0.5) / 2.0 ** 23
+    return -np.log(-np.log(u))
+
+
+def test_sampled_rows_are_keyed_by_their_row_in_the_batch(oracle_lib):
+    """[VT] Step 4 draws one token per hidden state; the draw of hidden state
+    m uses noise index m, its row in the caller's batch.  A call over a
+    slice of the batch that starts at row j (m_base = j) must draw exactly
+    what those rows draw in the whole batch, and every drawn token's score
+    must be its s plus the generator's noise for its row and full id."""
+    M, d, V_high, k = 7, 32, 300, 4
+    seed, offset = (0x1234_5678_9ABC, (3 << 32) + 17)
+    Hh = synth.bf16_bits(synth.normal_bf16((M, d), 1.0, seed=31))
+    Wh = synth.bf16_bits(synth.normal_bf16((V_high, d), 0.2, seed=32))
+    t2f = synth.rank_permutation(900, 33)[:V_high].numpy()
+    whole = oracle.draft_head_ex(Hh, Wh, t2f, k, sample=True, seed=seed,
+                                 offset=offset, temperature=0.7)
+    for j, n in ((0, 1), (1, 2), (4, 3), (6, 1)):
+        part = oracle.draft_head_ex(np.ascontiguousarray(Hh[j:j + n]), Wh, t2f,
+                                    k, sample=True, seed=seed, offset=offset,
+                                    temperature=0.7, m_base=j)
+        assert np.array_equal(part["ids"], whole["ids"][j:j + n]), j
+        np.testing.assert_array_equal(part["scores"], whole["scores"][j:j + n])
+    g = whole["scores"] - whole["logits"] / 0.7
+    for m in range(M):
+        want = [philox_gumbel(seed, offset, m, int(f)) for f in whole["ids"][m]]
+        np.testing.assert_allclose(g[m], want, rtol=0, atol=1e-9)
+
+
 def test_steps_and_seeds_change_the_draw(oracle_lib):
     """Different offsets (steps) or seeds give different noise; the same
     (seed, offset) repeats it."""
