@@ -379,11 +379,16 @@ void vt_host_step_destroy(vt_host_step* h);
  * (inside a CUDA stream capture that must not gain allocation nodes, on
  * hosts that forbid allocation after start-up, or as a plugin confined to
  * another framework's memory pool), so they cannot provide the workspace
- * vt_draft_head needs.  This call computes exactly what vt_draft_head
- * computes, with the same arguments minus the workspace, and allocates
- * nothing: its scratch is one fixed 1 MiB array in device memory that the
- * library defines and every GPU that loads the library keeps until exit.
- * It always runs the GEMV kernel, four hidden states at a time.
+ * vt_draft_head needs.  This call computes what vt_draft_head computes,
+ * with the same arguments minus the workspace, and allocates nothing: its
+ * scratch is one fixed 1 MiB array in device memory that the library
+ * defines and every GPU that loads the library keeps until exit.
+ * It always runs the GEMV kernel, four hidden states at a time.  For M = 1
+ * that is vt_draft_head's own kernel.  For M >= 2 vt_draft_head uses the
+ * tensor-core path, which sums in another order, so the two calls agree
+ * within the head's tolerances (logits within 1e-3 * (1 + |logit|),
+ * probabilities within 1e-4), and their ids agree except where two
+ * candidates' logits are closer than that.
  *
  *   Limit     the GEMV scratch, 2048 + 4096 * min(M, 4) * P bytes with
  *             P = 4 + 2k rounded up to a multiple of 4, must fit in 1 MiB:
@@ -395,6 +400,14 @@ void vt_host_step_destroy(vt_host_step* h);
  *   Sharing   all calls on a device share the one array; calls that overlap
  *             on the GPU (unordered streams) race on it and give wrong
  *             results.  Calls on one stream are safe.
+ *   Timeouts  the kernel's one bounded wait (the final merge's copy of the
+ *             partial results, about a second) cannot be reported by this
+ *             call: its error word lies inside the private array and no
+ *             call returns it, nor clears it.  When that wait gives up the
+ *             call leaves the out_ids rows from the one it failed on
+ *             unwritten.  A caller that must detect this fills out_ids with
+ *             -1 before the call (no full-vocabulary id is negative) and
+ *             checks for -1 after synchronising.
  * ------------------------------------------------------------------------ */
 vt_status vt_draft_head_noalloc(const uint16_t* H, int32_t M, int32_t d,
                                 int64_t ldh, const uint16_t* W_high,

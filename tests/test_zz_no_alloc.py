@@ -5,10 +5,13 @@ Callers that may not allocate device memory where they run a draft step
 forbid allocation after start-up, or as plugins confined to someone else's
 memory pool) use this entry point; it keeps its scratch in a fixed device
 array inside the library instead of taking a workspace.  These tests call
-it through the C ABI and check it against vt_draft_head (the entry point
-with a caller-provided workspace) on two calls in a row, within the
-tolerances of the other head tests.  The file sorts last so that a run that
-stops at the first failure has already run every other test.
+it through the C ABI on two calls in a row and check each call against
+vt_draft_head (the entry point with a caller-provided workspace) within the
+tolerances of the other head tests, and its top-k against the oracle by
+the rule of the other head tests (ids may differ only where oracle logits
+are closer than the logit tolerance).  For M = 1 both entry points run the
+same kernel, so their ids must be equal.  The file sorts last so that a
+run that stops at the first failure has already run every other test.
 """
 import ctypes
 
@@ -16,8 +19,10 @@ import pytest
 import torch
 
 import frequency_ranked_drafter_gb300 as vt
+import oracle
 import synth
-from gpu_util import LOGIT_RTOL, PROB_ATOL, need_cuda
+from gpu_util import (LOGIT_RTOL, PROB_ATOL, bits_host, check_logits,
+                      check_topk, need_cuda)
 
 pytestmark = pytest.mark.gpu
 
@@ -59,14 +64,23 @@ def test_noalloc_matches_workspace_entry_point(d, V, V_high, M, k):
     t2f = synth.rank_permutation(V, 33)[:V_high].to(dev)
     ref_logits = torch.empty(M, V_high, dtype=torch.float32, device=dev)
     ref_ids, ref_probs = vt.draft_head(H, W_high, t2f, k, out_logits=ref_logits)
+    Hh, Wh, t2f_h = bits_host(H), bits_host(W_high), t2f.cpu().numpy()
+    o_ref = oracle.draft_head(Hh, Wh, t2f_h, k)
+    o_logits = oracle.head_logits(Hh, Wh)
     for call in range(2):  # two calls in a row share the same scratch
         rc, ids, probs, logits = run_noalloc(fn, H, W_high, t2f, k)
         assert rc == VT_OK, lib.vt_last_error()
         torch.cuda.synchronize()
-        assert torch.equal(ids, ref_ids), f"call {call}: ids differ"
-        assert (probs - ref_probs).abs().max().item() <= PROB_ATOL
+        # against the workspace entry point: same results within tolerance
         tol = LOGIT_RTOL * (1.0 + ref_logits.abs())
-        assert ((logits - ref_logits).abs() <= tol).all()
+        assert ((logits - ref_logits).abs() <= tol).all(), f"call {call}"
+        assert (probs - ref_probs).abs().max().item() <= PROB_ATOL
+        if M == 1:  # the same GEMV kernel: the same ids
+            assert torch.equal(ids, ref_ids), f"call {call}: ids differ"
+        # against the oracle
+        check_logits(logits.cpu().numpy(), o_logits)
+        check_topk(ids.cpu().numpy(), probs.cpu().numpy(), o_logits, t2f_h,
+                   o_ref, k)
 
 
 def test_noalloc_rejects_scratch_beyond_its_limit():
