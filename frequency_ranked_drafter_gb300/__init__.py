@@ -25,7 +25,7 @@ from . import build as _build
 
 __all__ = ["VTError", "load", "library_path", "count_tokens", "select_vocab",
            "gather_rows", "draft_head", "draft_head_host", "build_vocab",
-           "coverage", "Workspace", "workspace_bytes"]
+           "coverage", "Workspace", "workspace_bytes", "check_error_word"]
 
 VT_OK = 0
 _STATUS = {0: "VT_OK", 1: "VT_ERR_INVALID_ARG", 2: "VT_ERR_CUDA",
@@ -94,6 +94,8 @@ def load(build_if_missing: bool = True):
                                      ctypes.POINTER(p)], ctypes.c_int),
             "vt_host_step_run": ([p, p, p, p], ctypes.c_int),
             "vt_host_step_staging": ([p], p),
+            "vt_host_step_error_word": ([p], p),
+            "vt_workspace_size": ([i32, i32, i32, i32], sz),
             "vt_host_step_destroy": ([p], None),
             "vt_draft_head_sets_workspace_size": ([i32, i32, i32, i32, p], sz),
             "vt_draft_head_sets": ([p, i32, i32, i64, p, i32, p, p, p, p, i32,
@@ -114,6 +116,23 @@ def _check(fn: str, status: int):
     if status != VT_OK:
         why = load().vt_last_error().decode(errors="replace")
         raise VTError(fn, status, why)
+
+
+VT_ERR_TIMEOUT = 5
+_ERR_WORD = 128  # byte offset of the device error word in every workspace
+
+
+def check_error_word(fn: str, ws: torch.Tensor):
+    """Reads the device error word of a call's workspace (synchronising
+    with the workspace's device), writes 0 back if it was set and raises
+    VTError(VT_ERR_TIMEOUT): a bounded wait inside that call's kernels gave
+    up, and its outputs are incomplete."""
+    word = ws[_ERR_WORD:_ERR_WORD + 4].view(torch.int32)
+    e = int(word.item())
+    if e != 0:
+        word.zero_()
+        raise VTError(fn, e, "a bounded wait inside the kernels gave up; "
+                             "the call's outputs are incomplete")
 
 
 def _ptr(t: torch.Tensor | None):
@@ -158,18 +177,17 @@ class Workspace:
 _ws = Workspace()
 
 
+_OPS = {"count": 0, "select": 1, "head": 2, "q": 3}
+
+
 def workspace_bytes(op: str, V: int = 0, M: int = 1, k: int = 1,
                     V_high: int = 1) -> int:
-    """Workspace size of op "count" (V), "select" (V) or "head" (M, V_high,
-    k)."""
-    lib = load()
-    if op == "count":
-        return lib.vt_count_tokens_workspace_size(V)
-    if op == "select":
-        return lib.vt_select_vocab_workspace_size(V)
-    if op == "head":
-        return lib.vt_draft_head_workspace_size(M, V_high, k)
-    raise ValueError(op)
+    """Workspace size (vt_workspace_size) of op "count" (V), "select" (V),
+    "head" (M, V_high, k) or "q" (M)."""
+    if op not in _OPS:
+        raise ValueError(op)
+    n = V if op in ("count", "select") else V_high
+    return load().vt_workspace_size(_OPS[op], M, n, k)
 
 
 def count_tokens(tokens: torch.Tensor, V: int, counts: torch.Tensor | None = None,
@@ -196,9 +214,12 @@ def count_tokens(tokens: torch.Tensor, V: int, counts: torch.Tensor | None = Non
 
 
 def select_vocab(counts: torch.Tensor, V_high: int,
-                 ws: torch.Tensor | None = None, out: tuple | None = None):
+                 ws: torch.Tensor | None = None, out: tuple | None = None,
+                 check: bool = False):
     """Top-V_high ids by count (ties: lower id).  Returns (t2f int32[V_high],
-    f2t int32[V] with -1 for dropped ids, sums int64[2] = [kept, total])."""
+    f2t int32[V] with -1 for dropped ids, sums int64[2] = [kept, total]).
+    ``check=True`` synchronises and raises VTError(VT_ERR_TIMEOUT) if a
+    bounded wait of the selection gave up."""
     _cuda(counts, "counts", torch.uint32)
     dev = counts.device
     V = counts.numel()
@@ -215,6 +236,8 @@ def select_vocab(counts: torch.Tensor, V_high: int,
     _check("vt_select_vocab", lib.vt_select_vocab(
         _ptr(counts), V, V_high, _ptr(t2f), _ptr(f2t), _ptr(sums), _ptr(ws),
         ws.numel(), _stream(dev)))
+    if check:
+        check_error_word("vt_select_vocab", ws)
     return t2f, f2t, sums
 
 
@@ -248,9 +271,13 @@ def draft_head(H: torch.Tensor, W_high: torch.Tensor, t2f: torch.Tensor | None,
                out_logits: torch.Tensor | None = None,
                ws: torch.Tensor | None = None, *,
                bias: torch.Tensor | None = None, temperature: float = 1.0,
-               sample: bool = False, seed: int = 0, offset: int = 0):
+               sample: bool = False, seed: int = 0, offset: int = 0,
+               check: bool = False):
     """One draft step: top-k full-vocabulary ids and softmax probabilities
     over the V_high kept rows for each of the M hidden states in ``H``.
+    ``check=True`` synchronises after the call, and raises
+    VTError(VT_ERR_TIMEOUT) (clearing the word) if a bounded wait inside the
+    head's kernels gave up.
 
     With options (vt_draft_head_ex): ``bias`` (fp32 [V_high]) is added to
     every logit, probabilities are softmax(logit / temperature), and
@@ -283,6 +310,8 @@ def draft_head(H: torch.Tensor, W_high: torch.Tensor, t2f: torch.Tensor | None,
             _ptr(H), M, d, H.stride(0), _ptr(W_high), V_high, _ptr(t2f), k,
             _ptr(out_ids), _ptr(out_probs), _ptr(out_logits), _ptr(ws),
             ws.numel(), _stream(dev)))
+        if check:
+            check_error_word("vt_draft_head", ws)
         return out_ids, out_probs
     if bias is not None:
         _cuda(bias, "bias", torch.float32)
@@ -295,6 +324,8 @@ def draft_head(H: torch.Tensor, W_high: torch.Tensor, t2f: torch.Tensor | None,
         _ptr(H), M, d, H.stride(0), _ptr(W_high), V_high, _ptr(t2f), k,
         ctypes.byref(opts), _ptr(out_ids), _ptr(out_probs), _ptr(out_logits),
         _ptr(ws), ws.numel(), _stream(dev)))
+    if check:
+        check_error_word("vt_draft_head_ex", ws)
     return out_ids, out_probs
 
 
@@ -322,7 +353,7 @@ def draft_head_sets(H: torch.Tensor, set_of_row, W_high_sets, t2f_sets, k: int,
                     sample: bool = False, seed: int = 0, offset: int = 0,
                     out_ids: torch.Tensor | None = None,
                     out_probs: torch.Tensor | None = None,
-                    ws: torch.Tensor | None = None):
+                    ws: torch.Tensor | None = None, check: bool = False):
     """One draft step where hidden state m uses kept vocabulary set
     ``set_of_row[m]`` (``W_high_sets[s]``, ``t2f_sets[s]``, optional
     ``bias_sets[s]``); otherwise as draft_head."""
@@ -362,6 +393,8 @@ def draft_head_sets(H: torch.Tensor, set_of_row, W_high_sets, t2f_sets, k: int,
         _ptr(H), M, d, H.stride(0), sor, S, W_arr, V_arr, T_arr, B_arr, k,
         ctypes.byref(opts), _ptr(out_ids), _ptr(out_probs), _ptr(ws),
         ws.numel(), _stream(dev)))
+    if check:
+        check_error_word("vt_draft_head_sets", ws)
     return out_ids, out_probs
 
 
@@ -469,6 +502,12 @@ class HostDraftHead:
         self.ids = torch.empty(M, k, dtype=torch.int32)
         self.probs = torch.empty(M, k, dtype=torch.float32)
         self._lib = lib
+
+    @property
+    def error_word(self) -> int:
+        """Device address of the handle's error word (uint32): a step whose
+        head finds it set raises VTError(VT_ERR_TIMEOUT) and clears it."""
+        return self._lib.vt_host_step_error_word(self._h)
 
     def __call__(self, H_host: torch.Tensor | None = None):
         src = self.H_host if H_host is None else H_host.contiguous()

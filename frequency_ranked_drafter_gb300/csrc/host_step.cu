@@ -11,9 +11,12 @@
 // while H crosses, and waits for the copy before reading it), then
 // vt_draft_head_ex, whose last CTA writes ids and probabilities straight into
 // a pinned host buffer (pinned memory is addressable from the device, so no
-// copy node follows).  Each step is then a host copy of H into the staging
-// buffer, one graph launch, one synchronise (which also makes the kernel's
-// host writes visible) and a host copy out.
+// copy node follows).  A last small kernel, a programmatic dependent of the
+// head (its launch overlaps the head), waits for the head to complete and
+// moves the head's device error word into the same pinned buffer, clearing
+// it.  Each step is then a host copy of H into the staging buffer, one graph
+// launch, one synchronise (which also makes the kernels' host writes
+// visible), a look at the error word and a host copy out.
 // The pages have no counterpart: it serves the end-to-end use of the head.
 #include <cstring>
 #include <new>
@@ -26,7 +29,8 @@ struct vt_host_step {
   cudaGraphExec_t exec = nullptr;
   uint16_t* H_pinned = nullptr;   // host, pinned [M, d]
   int32_t* out_pinned = nullptr;  // host, pinned [2, M, k] (ids, prob bits),
-                                  // written by the head's kernel
+                                  // written by the head's kernel, then the
+                                  // head's error word
   uint16_t* H_dev = nullptr;      // device [M, d]
   void* ws = nullptr;             // device head workspace
 };
@@ -44,6 +48,16 @@ __global__ void __launch_bounds__(kCopyThreads)
   for (int i = blockIdx.x * kCopyThreads + threadIdx.x; i < n;
        i += gridDim.x * kCopyThreads)
     dst[i] = src[i];
+}
+
+// *err_out = *err; *err = 0, once the head before it has completed
+// (err_out in pinned host memory: a plain store, read after the step's
+// synchronise).
+__global__ void host_err_publish_kernel(unsigned* err, unsigned* err_out) {
+  vt::grid_dependency_wait();
+  const unsigned e = *err;
+  *err_out = e;
+  if (e) *err = 0u;
 }
 
 void destroy(vt_host_step* h) {
@@ -79,7 +93,7 @@ extern "C" vt_status vt_host_step_create(const uint16_t* W_high, int32_t V_high,
   h->M = M;
   h->d = d;
   h->k = k;
-  const size_t hbytes = (size_t)M * d * 2, obytes = (size_t)M * k * 8;
+  const size_t hbytes = (size_t)M * d * 2, obytes = (size_t)M * k * 8 + 4;
   const size_t wbytes = vt_draft_head_workspace_size(M, V_high, k);
   auto bad = [&](const char* what) {
     const cudaError_t e = cudaGetLastError();
@@ -103,6 +117,8 @@ extern "C" vt_status vt_host_step_create(const uint16_t* W_high, int32_t V_high,
     return bad("output buffer mapping");
   int32_t* ids_dev = out_devp;
   float* probs_dev = reinterpret_cast<float*>(out_devp + (size_t)M * k);
+  unsigned* err_out = reinterpret_cast<unsigned*>(out_devp + (size_t)2 * M * k);
+  unsigned* err_dev = reinterpret_cast<unsigned*>(static_cast<char*>(h->ws) + 128);
   uint16_t* H_src = nullptr;
   if (cudaHostGetDevicePointer((void**)&H_src, h->H_pinned, 0) != cudaSuccess)
     return bad("staging buffer mapping");
@@ -116,9 +132,19 @@ extern "C" vt_status vt_host_step_create(const uint16_t* W_high, int32_t V_high,
     host_h_copy_kernel<<<copy_blocks, kCopyThreads, 0, h->stream>>>(
         reinterpret_cast<const uint4*>(H_src), reinterpret_cast<uint4*>(h->H_dev), n16);
     if (cudaGetLastError() != cudaSuccess) return bad("copy in");
-    const vt_status st = vt_draft_head_ex(h->H_dev, M, d, d, W_high, V_high, t2f, k,
-                                          opts, ids_dev, probs_dev, nullptr, h->ws,
-                                          wbytes, h->stream);
+    vt_status st = vt_draft_head_ex(h->H_dev, M, d, d, W_high, V_high, t2f, k,
+                                    opts, ids_dev, probs_dev, nullptr, h->ws,
+                                    wbytes, h->stream);
+    if (st == VT_OK) {
+      const cudaError_t pe = launch_dependent(host_err_publish_kernel, dim3(1),
+                                              dim3(1), 0, h->stream, err_dev,
+                                              err_out);
+      if (pe != cudaSuccess) {
+        cudaGetLastError();
+        st = fail(VT_ERR_CUDA, std::string("host_err_publish_kernel: ") +
+                                   cudaGetErrorString(pe));
+      }
+    }
     if (st != VT_OK) {
       if (pass == 1) {
         cudaGraph_t g = nullptr;
@@ -153,6 +179,11 @@ extern "C" vt_status vt_host_step_run(vt_host_step* h, const uint16_t* H_host,
       cudaStreamSynchronize(h->stream) != cudaSuccess)
     return fail(VT_ERR_CUDA, std::string("vt_host_step_run: ") +
                                  cudaGetErrorString(cudaGetLastError()));
+  const unsigned err = reinterpret_cast<volatile unsigned*>(h->out_pinned)[2 * mk];
+  if (err != 0)
+    return fail(VT_ERR_TIMEOUT,
+                "vt_host_step_run: a bounded wait inside the head gave up; "
+                "the step's outputs are incomplete");
   std::memcpy(ids_host, h->out_pinned, mk * 4);
   std::memcpy(probs_host, h->out_pinned + mk, mk * 4);
   return VT_OK;
@@ -160,6 +191,10 @@ extern "C" vt_status vt_host_step_run(vt_host_step* h, const uint16_t* H_host,
 
 extern "C" uint16_t* vt_host_step_staging(vt_host_step* h) {
   return h ? h->H_pinned : nullptr;
+}
+
+extern "C" uint32_t* vt_host_step_error_word(vt_host_step* h) {
+  return h ? reinterpret_cast<uint32_t*>(static_cast<char*>(h->ws) + 128) : nullptr;
 }
 
 extern "C" void vt_host_step_destroy(vt_host_step* h) {

@@ -226,12 +226,13 @@ __global__ void __launch_bounds__(kSelThreads, 1) onesweep_kernel(PassArgs a) {
   }
 }
 
-// Workspace: keys/values ping-pong, then a zero-initialised block (digit
-// histograms, per-pass tile status, tile counters, error word) that one
-// memset clears at the start of every call.
+// Workspace: a zero-initialised block (a 256-byte header whose 32-bit word
+// at byte 128 is the error word, as in the head's workspace; digit
+// histograms; per-pass tile status; tile counters) that one memset clears
+// at the start of every call, then the keys/values ping-pong.
 struct SelectLayout {
-  size_t keys_a, vals_a, keys_b, vals_b, zero_begin, ghist, status, counters,
-      err, zero_end, total;
+  size_t zero_begin, err, ghist, status, counters, zero_end, keys_a, vals_a,
+      keys_b, vals_b, total;
 };
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -240,16 +241,16 @@ SelectLayout select_layout(int V) {
   const size_t T = (size_t)(V + kSelTile - 1) / kSelTile;
   SelectLayout L;
   size_t o = 0;
+  L.zero_begin = o;
+  L.err = o + 128; o += 256;
+  L.ghist = o;    o += round256(4 * 256 * 4);
+  L.status = o;   o += round256(4 * T * 256 * 4);
+  L.counters = o; o += 256;
+  L.zero_end = o;
   L.keys_a = o; o += round256((size_t)V * 4);
   L.vals_a = o; o += round256((size_t)V * 4);
   L.keys_b = o; o += round256((size_t)V * 4);
   L.vals_b = o; o += round256((size_t)V * 4);
-  L.zero_begin = o;
-  L.ghist = o;    o += round256(4 * 256 * 4);
-  L.status = o;   o += round256(4 * T * 256 * 4);
-  L.counters = o; o += 256;
-  L.err = o;      o += 256;
-  L.zero_end = o;
   L.total = o;
   return L;
 }

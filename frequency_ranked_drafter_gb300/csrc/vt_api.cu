@@ -93,6 +93,16 @@ const char* vt_status_string(int status) {
 
 const char* vt_last_error(void) { return vt::g_last_error.c_str(); }
 
-int vt_version(void) { return 100; }
+int vt_version(void) { return 101; }
+
+size_t vt_workspace_size(int32_t op, int32_t M, int32_t n, int32_t k) {
+  switch (op) {
+    case VT_OP_COUNT: return vt_count_tokens_workspace_size(n);
+    case VT_OP_SELECT: return vt_select_vocab_workspace_size(n);
+    case VT_OP_HEAD: return vt_draft_head_workspace_size(M, n, k);
+    case VT_OP_Q: return vt_draft_q_workspace_size(M);
+    default: return 0;
+  }
+}
 
 }  // extern "C"

@@ -35,6 +35,14 @@
  *   - Calls that take a workspace (`ws`) need one of at least the size the
  *     matching *_workspace_size function returns, 256-byte aligned.  Calls
  *     running concurrently (other streams) need distinct workspaces.
+ *   - Error words.  Kernels that wait on other CTAs or on their own copies
+ *     (vt_select_vocab's look-back, the head's merges and tensor-core
+ *     pipeline) bound every wait (about a second).  A wait that gives up
+ *     writes VT_ERR_TIMEOUT to the 32-bit word at byte 128 of the call's
+ *     workspace and the kernel returns; the call's outputs are then
+ *     incomplete.  The call itself has returned VT_OK by then (it is
+ *     asynchronous): read the word after synchronising the stream.
+ *     vt_host_step_run reads it for you and returns VT_ERR_TIMEOUT.
  */
 #ifndef VT_H_
 #define VT_H_
@@ -52,7 +60,7 @@ typedef enum vt_status {
   VT_ERR_CUDA = 2,        /* a CUDA runtime call or launch failed */
   VT_ERR_UNSUPPORTED = 3, /* valid but outside what this build supports */
   VT_ERR_WORKSPACE = 4,   /* workspace missing, too small or misaligned */
-  VT_ERR_TIMEOUT = 5      /* reserved: a bounded device wait gave up */
+  VT_ERR_TIMEOUT = 5      /* a bounded device wait gave up (see error words) */
 } vt_status;
 
 /* Static string naming a status code. */
@@ -64,6 +72,26 @@ const char* vt_last_error(void);
 
 /* Library ABI version (major * 100 + minor). */
 int vt_version(void);
+
+/* ------------------------------------------------------------------------
+ * vt_workspace_size — workspace bytes of one operation, in one call; the
+ * same numbers as the per-operation *_workspace_size functions below.
+ *
+ *   op  VT_OP_COUNT  (vt_count_tokens):  n = V, the vocabulary size;
+ *       VT_OP_SELECT (vt_select_vocab):  n = V;
+ *       VT_OP_HEAD   (vt_draft_head, vt_draft_head_ex): M, n = V_high, k;
+ *       VT_OP_Q      (vt_draft_q):       M.
+ *   Arguments an operation does not use are ignored.  Returns 0 for an
+ *   unknown op or sizes out of range.  (vt_draft_head_sets takes per-set
+ *   sizes: use vt_draft_head_sets_workspace_size.)
+ * ------------------------------------------------------------------------ */
+typedef enum {
+  VT_OP_COUNT = 0,
+  VT_OP_SELECT = 1,
+  VT_OP_HEAD = 2,
+  VT_OP_Q = 3
+} vt_op;
+size_t vt_workspace_size(int32_t op, int32_t M, int32_t n, int32_t k);
 
 /* ------------------------------------------------------------------------
  * vt_count_tokens — token-frequency histogram.
@@ -102,7 +130,11 @@ vt_status vt_count_tokens(const int32_t* tokens, int64_t n, int32_t V,
  *             the kept ids' counts and of all counts.  Coverage is
  *             (double)kept / (double)total, computed by the caller after
  *             the stream is synchronised (NaN when total == 0).
- *   ws        (device) workspace of vt_select_vocab_workspace_size(V) bytes.
+ *   ws        (device) workspace of vt_select_vocab_workspace_size(V) bytes;
+ *             no zero-fill needed.  Its 32-bit word at byte 128 is the
+ *             call's error word: cleared when the call starts, then 0, or
+ *             VT_ERR_TIMEOUT if a look-back wait gave up (t2f, f2t and sums
+ *             are then incomplete).
  * ------------------------------------------------------------------------ */
 size_t vt_select_vocab_workspace_size(int32_t V);
 vt_status vt_select_vocab(const uint32_t* counts, int32_t V, int32_t V_high,
@@ -172,7 +204,8 @@ vt_status vt_gather_bias(const float* b, int64_t V, const int32_t* t2f,
  *             out_logits is NULL).  On every path the 32-bit word at byte
  *             128 is a device error word: 0, or VT_ERR_TIMEOUT if a bounded
  *             wait inside the kernel gave up (readable after a synchronise;
- *             the outputs of that call are then incomplete).
+ *             the outputs of that call are then incomplete).  The head never
+ *             clears it: a caller that reads a non-zero word writes 0 back.
  *
  * Paths: M = 1 runs a split-V GEMV (CUDA cores, one launch); M >= 2 runs a
  * tcgen05 tensor-core GEMM over all M rows at once plus a per-row softmax
@@ -277,7 +310,8 @@ vt_status vt_draft_noise(uint64_t seed, uint64_t offset, int32_t m,
  *               entries), fp32 [V_high_sets[s]], 4-byte aligned.
  *   ws          (device) vt_draft_head_sets_workspace_size(M, d, k, S,
  *               V_high_sets) bytes, 256-byte aligned, zero-filled once
- *               before its first use.
+ *               before its first use.  It begins with the head's workspace,
+ *               so its error word is the head's (byte 128).
  * For each set in use: one gather of its rows' hidden states, the head
  * (GEMV for one row, tensor cores for more), one scatter of its outputs.
  * All sets are checked before anything is launched.
@@ -357,9 +391,15 @@ vt_status vt_selftest_wait_timeout(uint32_t* err_word, int64_t budget_cycles,
  *   vt_host_step_run: copies H_host (host, bf16 [M, d]; skipped when it is
  *     the staging buffer) into the staging buffer, launches the graph,
  *     synchronises the handle's stream and writes ids_host [M, k] and
- *     probs_host [M, k] (host).  Not thread-safe per handle.
+ *     probs_host [M, k] (host).  The graph ends with a small kernel that
+ *     moves the head's error word (byte 128 of the handle's workspace) into
+ *     the pinned output buffer and clears it: if a bounded wait inside the
+ *     head gave up, the call returns VT_ERR_TIMEOUT and writes nothing.
+ *     Not thread-safe per handle.
  *   vt_host_step_staging: the pinned [M, d] staging buffer (write H there to
  *     skip the host copy).
+ *   vt_host_step_error_word: the device address of the handle's error word
+ *     (uint32), for tools and tests of the failure path.
  *   vt_host_step_destroy: synchronises and frees everything (NULL is a no-op).
  * ------------------------------------------------------------------------ */
 typedef struct vt_host_step vt_host_step;
@@ -369,6 +409,7 @@ vt_status vt_host_step_create(const uint16_t* W_high, int32_t V_high, int32_t d,
 vt_status vt_host_step_run(vt_host_step* h, const uint16_t* H_host,
                            int32_t* ids_host, float* probs_host);
 uint16_t* vt_host_step_staging(vt_host_step* h);
+uint32_t* vt_host_step_error_word(vt_host_step* h);
 void vt_host_step_destroy(vt_host_step* h);
 
 /* ------------------------------------------------------------------------

@@ -1,7 +1,13 @@
-"""Helpers shared by the GPU parity tests (comparison rules, host copies)."""
+"""Helpers shared by the GPU parity tests (comparison rules, host copies,
+the oracle over many rows)."""
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import pytest
 import torch
+
+import oracle
 
 # Tolerances of the trimmed head (bf16 inputs, fp32 accumulation):
 #   |logit_gpu - logit_oracle| <= 1e-3 * (1 + |logit_oracle|)
@@ -82,3 +88,54 @@ def check_topk(ids, probs, ref_logits, t2f, oracle_res, k, extra=None):
                 f"row {m} rank {r}: prob {probs[m, r]} vs {p_ref}")
         exact += int(list(g) == o_ids.tolist())
     return exact
+
+
+def _row_chunks(M: int):
+    n = max(1, min(M, os.cpu_count() or 1))
+    step = (M + n - 1) // n
+    return [(a, min(M, a + step)) for a in range(0, M, step)]
+
+
+def oracle_head(Hh: np.ndarray, Wh: np.ndarray, t2f_h, k: int, logits=True,
+                **opts):
+    """The oracle's draft step for every row of ``Hh`` (and, with
+    ``logits``, its fp64 logits [M, V_high]), run over chunks of rows in
+    threads: the oracle treats rows independently and ctypes releases the
+    GIL during each call, so the joined result equals one call over all rows.
+    With ``opts`` (bias, temperature, sample, seed, offset, m_base) the
+    oracle's draft_head_ex is used, each chunk starting at its own row
+    (m_base counts the rows of the whole call)."""
+    M = Hh.shape[0]
+    chunks = _row_chunks(M)
+    base = opts.pop("m_base", 0)
+
+    def step(c):
+        a, b = c
+        Hc = np.ascontiguousarray(Hh[a:b])
+        if opts:
+            r = oracle.draft_head_ex(Hc, Wh, t2f_h, k, m_base=base + a, **opts)
+        else:
+            r = oracle.draft_head(Hc, Wh, t2f_h, k)
+        return r, (oracle.head_logits(Hc, Wh) if logits else None)
+
+    with ThreadPoolExecutor(len(chunks)) as ex:
+        parts = list(ex.map(step, chunks))
+    ref = {key: np.concatenate([p[0][key] for p in parts])
+           for key in parts[0][0]}
+    full = np.concatenate([p[1] for p in parts]) if logits else None
+    return ref, full
+
+
+def oracle_q(Hh: np.ndarray, Wh: np.ndarray, t2f_h, V: int, **opts):
+    """The oracle's full-vocabulary q [M, V] for every row of ``Hh``, over
+    chunks of rows in threads (rows are independent; the joined result
+    equals one call)."""
+    chunks = _row_chunks(Hh.shape[0])
+
+    def step(c):
+        a, b = c
+        return oracle.draft_q(np.ascontiguousarray(Hh[a:b]), Wh, t2f_h, V,
+                              **opts)
+
+    with ThreadPoolExecutor(len(chunks)) as ex:
+        return np.concatenate(list(ex.map(step, chunks)))

@@ -57,6 +57,40 @@ def test_workspace_sizes(lib):
     assert lib.vt_draft_head_workspace_size(0, 32768, 10) == 0
 
 
+def test_workspace_size_dispatcher_matches_the_per_op_functions(lib):
+    """vt_workspace_size(op, M, n, k) returns what each operation's own size
+    function returns (n is V for the histogram and the selection, V_high for
+    the head), and 0 for an unknown op."""
+    COUNT, SELECT, HEAD, Q = 0, 1, 2, 3
+    for V in (1, 4096, 128256, 300000):
+        assert lib.vt_workspace_size(COUNT, 0, V, 0) == \
+            lib.vt_count_tokens_workspace_size(V)
+        assert lib.vt_workspace_size(SELECT, 7, V, 3) == \
+            lib.vt_select_vocab_workspace_size(V)
+    for M, V_high, k in ((1, 32768, 10), (4, 1000, 32), (60, 8192, 10),
+                         (256, 128256, 1), (0, 10, 1)):
+        assert lib.vt_workspace_size(HEAD, M, V_high, k) == \
+            lib.vt_draft_head_workspace_size(M, V_high, k)
+        assert lib.vt_workspace_size(Q, M, 0, 0) == \
+            lib.vt_draft_q_workspace_size(M)
+    assert lib.vt_workspace_size(4, 1, 1, 1) == 0
+    assert lib.vt_workspace_size(-1, 1, 1, 1) == 0
+    assert vt.workspace_bytes("head", M=60, V_high=8192, k=10) == \
+        lib.vt_draft_head_workspace_size(60, 8192, 10)
+
+
+def test_workspaces_hold_the_error_word_at_byte_128(lib):
+    """Every workspace that has an error word keeps it at byte 128, so
+    workspaces are at least 132 bytes."""
+    assert lib.vt_select_vocab_workspace_size(1) >= 132
+    assert lib.vt_draft_head_workspace_size(1, 1, 1) >= 132
+    assert lib.vt_draft_head_workspace_size(2, 1, 1) >= 132
+
+
+def test_host_step_error_word_of_null_handle(lib):
+    assert lib.vt_host_step_error_word(None) is None
+
+
 def test_draft_head_rejects_bad_arguments(lib):
     ws_ok = lib.vt_draft_head_workspace_size(1, 32768, 10)
 

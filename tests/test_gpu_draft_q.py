@@ -10,7 +10,7 @@ import torch
 import frequency_ranked_drafter_gb300 as vt
 import oracle
 import synth
-from gpu_util import PROB_ATOL, bits_host, need_cuda
+from gpu_util import PROB_ATOL, bits_host, need_cuda, oracle_q
 
 pytestmark = pytest.mark.gpu
 
@@ -21,8 +21,8 @@ def f2t_of(t2f_h: np.ndarray, V: int) -> np.ndarray:
     return f2t
 
 
-def run_q(d, V, V_high, M, seed, T=1.0, use_bias=False, identity=False,
-          rows=None):
+def run_q(d, V, V_high, M, seed, T=1.0, use_bias=False, identity=False):
+    """Every row of q against the oracle."""
     dev = need_cuda()
     W = synth.normal_bf16((V_high, d), 0.02, seed=seed, device=dev)
     H = synth.normal_bf16((M, d), 1.0, seed=seed + 1, device=dev)
@@ -40,10 +40,9 @@ def run_q(d, V, V_high, M, seed, T=1.0, use_bias=False, identity=False,
     vt.draft_head(H, W, t2f, 1, out_logits=logits, bias=bias, temperature=T)
     q = vt.draft_q(logits, f2t, V, temperature=T)
     torch.cuda.synchronize()
-    rows = list(range(M)) if rows is None else rows
-    ref = oracle.draft_q(bits_host(H[rows]), bits_host(W), t2f_h, V, bias=b_h,
-                         temperature=T)
-    got = q.cpu().numpy()[rows].astype(np.float64)
+    ref = oracle_q(bits_host(H), bits_host(W), t2f_h, V, bias=b_h,
+                   temperature=T)
+    got = q.cpu().numpy().astype(np.float64)
     assert np.abs(got - ref).max() <= PROB_ATOL
     if t2f_h is not None:
         dropped = np.setdiff1d(np.arange(V), t2f_h)
@@ -73,8 +72,9 @@ def test_q_full_size_llama3_8b():
     run_q(4096, 128256, 32768, 1, seed=1002)
 
 
-def test_q_tree_m60_sampled_rows():
-    run_q(4096, 128256, 32768, 60, seed=1003, T=0.9, rows=[0, 29, 59])
+def test_q_tree_m60_every_row():
+    """The EAGLE-2 tree step: q of all 60 nodes over V = 128256."""
+    run_q(4096, 128256, 32768, 60, seed=1003, T=0.9)
 
 
 def test_q_at_drawn_tokens_is_the_reported_probability():

@@ -11,13 +11,13 @@ import frequency_ranked_drafter_gb300 as vt
 import oracle
 import synth
 from gpu_util import (bits_host, check_logits, check_topk, fp32_sum_bound,
-                      need_cuda)
+                      need_cuda, oracle_head)
 
 pytestmark = pytest.mark.gpu
 
 
 def run_case(d, V_high, M, k, seed, hs=1.0, ws=0.02, use_t2f=True,
-             V=None, ldh=None, want_logits=True, check_rows=None, widen=False):
+             V=None, ldh=None, want_logits=True, widen=False):
     dev = need_cuda()
     V = V or max(V_high, 2 * V_high)
     W_high = synth.normal_bf16((V_high, d), ws, seed=seed, device=dev)
@@ -33,18 +33,16 @@ def run_case(d, V_high, M, k, seed, hs=1.0, ws=0.02, use_t2f=True,
     ids, probs = vt.draft_head(H, W_high, t2f, k, out_logits=logits, ws=wsb)
     torch.cuda.synchronize()
     assert int(wsb[128:132].view(torch.int32).item()) == 0, "device error word"
-    rows = list(range(M)) if check_rows is None else check_rows
-    Hh = bits_host(H[rows])
+    Hh = bits_host(H)
     Wh = bits_host(W_high)
     t2f_h = None if t2f is None else t2f.cpu().numpy()
-    ref = oracle.draft_head(Hh, Wh, t2f_h, k)
-    ref_logits = oracle.head_logits(Hh, Wh)
+    ref, ref_logits = oracle_head(Hh, Wh, t2f_h, k)
     extra = fp32_sum_bound(Hh, Wh) if widen else None
     if want_logits:
-        check_logits(logits.cpu().numpy()[rows], ref_logits,
+        check_logits(logits.cpu().numpy(), ref_logits,
                      0.0 if extra is None else extra)
-    exact = check_topk(ids.cpu().numpy()[rows], probs.cpu().numpy()[rows],
-                       ref_logits, t2f_h, ref, k, extra)
+    exact = check_topk(ids.cpu().numpy(), probs.cpu().numpy(), ref_logits,
+                       t2f_h, ref, k, extra)
     return exact, ids, probs
 
 
@@ -172,12 +170,11 @@ def test_qwen_and_llama1b_heads(shape, M):
     run_case(shape.d, shape.V_high, M, shape.k, seed=shape.seed + M, V=shape.V)
 
 
-def test_tree_draft_m60_sampled_rows():
-    """M = 60 tree nodes at V_high = 32768: every row on the GPU, five
-    sampled rows against the oracle."""
+def test_tree_draft_m60_every_row():
+    """M = 60 tree nodes at V_high = 32768: every row against the oracle,
+    logits included."""
     cfg = synth.TREE_HEAD
-    run_case(cfg.d, cfg.V_high, cfg.M, cfg.k, seed=cfg.seed, V=cfg.V,
-             want_logits=False, check_rows=[0, 17, 31, 48, 59])
+    run_case(cfg.d, cfg.V_high, cfg.M, cfg.k, seed=cfg.seed, V=cfg.V)
 
 
 def test_host_draft_head_graph_steps():

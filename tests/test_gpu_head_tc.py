@@ -13,13 +13,14 @@ import frequency_ranked_drafter_gb300 as vt
 import oracle
 import synth
 from gpu_util import (bits_host, check_logits, check_topk, fp32_sum_bound,
-                      need_cuda)
+                      need_cuda, oracle_head)
 
 pytestmark = pytest.mark.gpu
 
 
-def run_tc(d, V_high, M, k, seed, rows=None, use_t2f=True, want_logits=True,
+def run_tc(d, V_high, M, k, seed, use_t2f=True, want_logits=True,
            hs=1.0, ws_scale=0.02, widen=False):
+    """Every hidden state of the call against the oracle."""
     dev = need_cuda()
     W_high = synth.normal_bf16((V_high, d), ws_scale, seed=seed, device=dev)
     H = synth.normal_bf16((M, d), hs, seed=seed + 1, device=dev)
@@ -33,17 +34,15 @@ def run_tc(d, V_high, M, k, seed, rows=None, use_t2f=True, want_logits=True,
     torch.cuda.synchronize()
     err = int(ws[128:132].view(torch.int32).item())
     assert err == 0, f"device error word {err}"
-    rows = list(range(M)) if rows is None else rows
-    Hh, Wh = bits_host(H[rows]), bits_host(W_high)
+    Hh, Wh = bits_host(H), bits_host(W_high)
     t2f_h = None if t2f is None else t2f.cpu().numpy()
-    ref = oracle.draft_head(Hh, Wh, t2f_h, k)
-    ref_logits = oracle.head_logits(Hh, Wh)
+    ref, ref_logits = oracle_head(Hh, Wh, t2f_h, k)
     extra = fp32_sum_bound(Hh, Wh) if widen else None
     if want_logits:
-        check_logits(logits.cpu().numpy()[rows], ref_logits,
+        check_logits(logits.cpu().numpy(), ref_logits,
                      0.0 if extra is None else extra)
-    check_topk(ids.cpu().numpy()[rows], probs.cpu().numpy()[rows], ref_logits,
-               t2f_h, ref, k, extra)
+    check_topk(ids.cpu().numpy(), probs.cpu().numpy(), ref_logits, t2f_h, ref,
+               k, extra)
     return ids, probs
 
 
@@ -82,24 +81,24 @@ def test_tc_repeated_calls_identical():
         assert torch.equal(ids, a[0]) and torch.equal(probs, a[1])
 
 
-def test_tc_eagle2_tree_m60_v_high_sweep():
+@pytest.mark.parametrize("V_high", [8192, 16384, 32768, 65536])
+def test_tc_eagle2_tree_m60_v_high_sweep(V_high):
     """EAGLE-2-style tree draft, d = 4096, M = 60, over the V_high sweep
-    (8192 .. 65536); four sampled hidden states against the oracle."""
-    for V_high in (8192, 16384, 32768, 65536):
-        run_tc(4096, V_high, 60, 10, seed=1003 + V_high, rows=[0, 21, 42, 59],
-               want_logits=False)
+    (8192 .. 65536): every hidden state against the oracle, logits
+    included."""
+    run_tc(4096, V_high, 60, 10, seed=1003 + V_high)
 
 
-def test_tc_full_vocab_m60_sampled():
-    run_tc(4096, 128256, 60, 10, seed=1003, rows=[7, 58], want_logits=False,
-           use_t2f=False)
+def test_tc_full_vocab_m60_every_row():
+    """The untrimmed end of the sweep (V = 128256, identity map), every
+    hidden state against the oracle."""
+    run_tc(4096, 128256, 60, 10, seed=1003, use_t2f=False)
 
 
 @pytest.mark.parametrize("shape", [synth.QWEN7B_HEAD, synth.LLAMA1B_HEAD])
 @pytest.mark.parametrize("M", [16, 64])
 def test_tc_qwen_and_llama1b_batch_sweep(shape, M):
-    run_tc(shape.d, shape.V_high, M, shape.k, seed=shape.seed + M,
-           rows=[0, M // 2, M - 1], want_logits=False)
+    run_tc(shape.d, shape.V_high, M, shape.k, seed=shape.seed + M)
 
 
 def test_gemv_and_tc_paths_share_one_workspace():
