@@ -16,9 +16,11 @@
 // swizzle) of the W tile and of H into a ring of shared-memory stages with
 // TMA (a stage is up to four such K blocks of the same rows, requested back
 // to back); one thread of warp 1 issues tcgen05.mma into a double-buffered TMEM
-// accumulator; warps 2-5 read finished accumulators out of TMEM and store
-// fp32 logits (tile rows along lanes, so every store is a coalesced 128-byte
-// row segment).  At these M the work stays bound by the W_high stream.
+// accumulator; warps 2-9 read finished accumulators out of TMEM (two warps
+// per 32-lane quadrant, alternate 32-column chunks, so the last tile's
+// epilogue, which nothing overlaps, takes half as long) and store fp32
+// logits (tile rows along lanes, so every store is a coalesced 128-byte row
+// segment).  At these M the work stays bound by the W_high stream.
 //
 // Softmax + top-k: each hidden state's V_high logits (L2-resident, bias
 // added by the GEMM epilogue) are split over CTAs of 4096; each CTA reduces
@@ -42,7 +44,10 @@
 namespace vt {
 namespace {
 
-constexpr int kTcThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
+// warp 0 TMA, warp 1 MMA + TMEM, warps 2-9 epilogue (two warps per TMEM lane
+// quadrant, each taking every other 32-column chunk of the accumulator)
+constexpr int kTcThreads = 320;
+constexpr int kTcEpilogueWarps = 8;
 constexpr int kTcMaxStages = 6;
 // k-blocks of a CTA's first W_high tile prefetched into L2 before the
 // dependency wait.
@@ -162,7 +167,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&tfull[b], 1);
-      tc::mbar_init(&tempty[b], 4);
+      tc::mbar_init(&tempty[b], kTcEpilogueWarps);
     }
     tc::mbar_init(&drain, 1);
     abort_flag = 0;
@@ -268,6 +273,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else {  // --------------------------------------------- epilogue warps
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int half = (warp - 2) >> 2;  // which chunks of the accumulator
     int it = 0;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
       const int acc = it & 1;
@@ -279,7 +285,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc::tc_fence_after();
       const int row = tile * kTcTileRows + 32 * q + lane;
       const float b = row < a.V_high && a.bias ? __ldg(a.bias + row) : 0.f;
-      for (int c0 = 0; c0 < a.N; c0 += 32) {
+      for (int c0 = 32 * half; c0 < a.N; c0 += 64) {
         float r[32];
         tc::tmem_ld_32x32(tmem + ((uint32_t)(32 * q) << 16) +
                               (uint32_t)(acc * a.NB + c0),
