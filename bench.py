@@ -501,7 +501,8 @@ def run_ours(args, world, rank, local):
     for Mq in (1, 60):
         lg = torch.randn(Mq, V_high, device=dev)
         qbuf = torch.empty(Mq, V, device=dev)
-        ws_q = torch.empty(max(256, 8 * Mq), dtype=torch.uint8, device=dev)
+        ws_q = torch.zeros(vt.workspace_bytes("q", M=Mq), dtype=torch.uint8,
+                           device=dev)
         t_q = max_over_ranks(graph_seconds(
             torch, lambda: vt.draft_q(lg, f2t, V, out=qbuf, ws=ws_q), 50),
             world)

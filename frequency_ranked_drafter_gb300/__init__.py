@@ -419,7 +419,7 @@ def draft_q(logits: torch.Tensor, f2t: torch.Tensor | None, V: int,
     lib = load()
     nbytes = lib.vt_draft_q_workspace_size(M)
     if ws is None:
-        ws = _ws.get("draft_q", nbytes, dev, zeroed=False)
+        ws = _ws.get("draft_q", nbytes, dev, zeroed=True)
     _check("vt_draft_q", lib.vt_draft_q(
         _ptr(logits), M, V_high, _ptr(f2t), V, float(temperature), _ptr(out),
         _ptr(ws), ws.numel(), _stream(dev)))

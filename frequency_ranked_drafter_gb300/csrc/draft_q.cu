@@ -162,19 +162,83 @@ __global__ void __launch_bounds__(kFillThreads)
 }
 
 // One kernel when a row of logits fits in shared memory: grid (P, M); every
-// CTA of row m stages the row's V_high logits in shared memory (coalesced
-// 16-byte loads), folds the row's (max, sum of exp) from there, then fills
-// its 1/P of q[m]: f2t in 16-byte vectors, the kept logits gathered from
-// shared memory (no L2 sector per gathered value), q in 16-byte stores.
+// CTA of row m stages the row's V_high values of logit / T in shared memory
+// (coalesced 16-byte loads) taking their maximum on the way, sums
+// exp(s - max) from shared memory in a second pass (no branch and one
+// exponential per value, where an online fold needed a compare and up to
+// two), then fills its 1/P of q[m], the kept values gathered from shared
+// memory (no L2 sector per gathered value), q in 16-byte stores.
+// Exponentials use the fast hardware form (relative error about 1e-6 here,
+// far inside the 1e-4 bound on q).
 constexpr int kRowQThreads = 1024;
+
+// Stages row m's logit / T in srow and returns (max, 1 / sum of exp(s -
+// max)) to every thread of the CTA.
+__device__ __forceinline__ float2 stage_row_stats(const float* __restrict__ row,
+                                                  int V_high, float inv_tau,
+                                                  float* srow) {
+  __shared__ float wm[kRowQThreads / 32], wsum[kRowQThreads / 32];
+  __shared__ float2 st_all;
+  float mm = -INFINITY;
+  if ((V_high & 3) == 0 && (reinterpret_cast<uintptr_t>(row) & 15) == 0) {
+    const float4* r4 = reinterpret_cast<const float4*>(row);
+    float4* s4 = reinterpret_cast<float4*>(srow);
+    const int n4 = V_high / 4;
+    constexpr int kBatch = 8;  // loads in flight per thread
+    for (int base = 0; base < n4; base += kRowQThreads * kBatch) {
+      float4 x[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int i = base + j * kRowQThreads + threadIdx.x;
+        if (i < n4) x[j] = __ldcg(r4 + i);
+      }
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int i = base + j * kRowQThreads + threadIdx.x;
+        if (i < n4) {
+          float4 y = x[j];
+          y.x *= inv_tau; y.y *= inv_tau; y.z *= inv_tau; y.w *= inv_tau;
+          s4[i] = y;
+          mm = fmaxf(mm, fmaxf(fmaxf(y.x, y.y), fmaxf(y.z, y.w)));
+        }
+      }
+    }
+  } else {
+    for (int i = threadIdx.x; i < V_high; i += kRowQThreads) {
+      const float x = __ldcg(row + i) * inv_tau;
+      srow[i] = x;
+      mm = fmaxf(mm, x);
+    }
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(~0u, mm, o));
+  if (lane == 0) wm[warp] = mm;
+  __syncthreads();  // also publishes the staged row
+  mm = wm[lane];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(~0u, mm, o));
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < V_high; i += kRowQThreads) ss += __expf(srow[i] - mm);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(~0u, ss, o);
+  if (lane == 0) wsum[warp] = ss;
+  __syncthreads();
+  if (warp == 0) {
+    ss = wsum[lane];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(~0u, ss, o);
+    if (lane == 0) st_all = make_float2(mm, 1.f / ss);
+  }
+  __syncthreads();
+  return st_all;
+}
 
 __global__ void __launch_bounds__(kRowQThreads, 1)
     q_row_kernel(const float* __restrict__ logits, int V_high,
                  const int32_t* __restrict__ f2t, int V, float inv_tau,
                  float* __restrict__ q, int span, bool vec) {
   extern __shared__ __align__(16) float srow[];  // [V_high] logit / T
-  __shared__ float wm[kRowQThreads / 32], wsum[kRowQThreads / 32];
-  __shared__ float2 st_all;
   const int m = blockIdx.y;
   const float* row = logits + (size_t)m * V_high;
   const int f_begin = blockIdx.x * span, f_end = min(V, f_begin + span);
@@ -197,67 +261,8 @@ __global__ void __launch_bounds__(kRowQThreads, 1)
   int idx[kFillIds];
   int f0 = f_begin + threadIdx.x * kFillIds;
   if (f0 < f_end) load_idx(f0, idx);
-  float mm = -INFINITY, ss = 0.f;
-  auto add = [&](float x) {
-    if (x > mm) {
-      ss = (ss > 0.f ? ss * expf(mm - x) : 0.f) + 1.f;
-      mm = x;
-    } else {
-      ss += expf(x - mm);
-    }
-  };
-  if ((V_high & 3) == 0 && (reinterpret_cast<uintptr_t>(row) & 15) == 0) {
-    const float4* r4 = reinterpret_cast<const float4*>(row);
-    float4* s4 = reinterpret_cast<float4*>(srow);
-    const int n4 = V_high / 4;
-    constexpr int kBatch = 8;  // loads in flight per thread
-    for (int base = 0; base < n4; base += kRowQThreads * kBatch) {
-      float4 x[kBatch];
-#pragma unroll
-      for (int j = 0; j < kBatch; ++j) {
-        const int i = base + j * kRowQThreads + threadIdx.x;
-        if (i < n4) x[j] = __ldcg(r4 + i);
-      }
-#pragma unroll
-      for (int j = 0; j < kBatch; ++j) {
-        const int i = base + j * kRowQThreads + threadIdx.x;
-        if (i < n4) {
-          float4 y = x[j];
-          y.x *= inv_tau; y.y *= inv_tau; y.z *= inv_tau; y.w *= inv_tau;
-          s4[i] = y;
-          add(y.x); add(y.y); add(y.z); add(y.w);
-        }
-      }
-    }
-  } else {
-    for (int i = threadIdx.x; i < V_high; i += kRowQThreads) {
-      const float x = __ldcg(row + i) * inv_tau;
-      srow[i] = x;
-      add(x);
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(~0u, mm, o);
-    const float s2 = __shfl_xor_sync(~0u, ss, o);
-    fold(mm, ss, m2, s2);
-  }
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (lane == 0) { wm[warp] = mm; wsum[warp] = ss; }
-  __syncthreads();  // also publishes the staged row
-  if (warp == 0) {
-    mm = wm[lane];
-    ss = wsum[lane];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float m2 = __shfl_xor_sync(~0u, mm, o);
-      const float s2 = __shfl_xor_sync(~0u, ss, o);
-      fold(mm, ss, m2, s2);
-    }
-    if (lane == 0) st_all = make_float2(mm, 1.f / ss);
-  }
-  __syncthreads();
-  const float mx = st_all.x, inv_sum = st_all.y;
+  const float2 st = stage_row_stats(row, V_high, inv_tau, srow);
+  const float mx = st.x, inv_sum = st.y;
   float* qm = q + (size_t)m * V;
   for (; f0 < f_end; f0 += kStep) {
     int nidx[kFillIds];
@@ -266,7 +271,7 @@ __global__ void __launch_bounds__(kRowQThreads, 1)
     float o[kFillIds];
 #pragma unroll
     for (int j = 0; j < kFillIds; ++j)
-      o[j] = (idx[j] >= 0 && idx[j] < V_high) ? expf(srow[idx[j]] - mx) * inv_sum : 0.f;
+      o[j] = (unsigned)idx[j] < (unsigned)V_high ? __expf(srow[idx[j]] - mx) * inv_sum : 0.f;
     if (full) {
       float4* dst = reinterpret_cast<float4*>(qm + f0);
       dst[0] = make_float4(o[0], o[1], o[2], o[3]);
@@ -324,9 +329,10 @@ extern "C" vt_status vt_draft_q(const float* logits, int32_t M, int32_t V_high,
     const int P = std::max(1, std::min(want, (V + per_part_min - 1) / per_part_min));
     int span = (V + P - 1) / P;
     span = (span + kFillIds - 1) / kFillIds * kFillIds;
+    const dim3 grid((V + span - 1) / span, M);
     if (!allow_max_smem(q_row_kernel, di)) return VT_ERR_CUDA;
-    q_row_kernel<<<dim3((V + span - 1) / span, M), kRowQThreads, row_bytes, s>>>(
-        logits, V_high, f2t, V, inv_tau, q, span, vec);
+    q_row_kernel<<<grid, kRowQThreads, row_bytes, s>>>(logits, V_high, f2t, V,
+                                                       inv_tau, q, span, vec);
     return launch_status("q_row_kernel");
   }
   float2* stats = static_cast<float2*>(ws);

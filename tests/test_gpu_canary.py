@@ -158,8 +158,12 @@ def test_draft_head_bounds(d, V_high, M, k, sample):
     assert torch.equal(ids2.t, ids.t)
 
 
-@pytest.mark.parametrize("V,V_high,M", [(5003, 1111, 3), (20001, 3001, 7),
-                                        (128256, 32768, 2)])
+@pytest.mark.parametrize("V,V_high,M", [
+    (5003, 1111, 3),      # V % 4 != 0: f2t read by each thread
+    (20001, 3001, 7),
+    (20004, 3001, 7),     # f2t through the shared-memory ring, ragged last chunk
+    (128256, 32768, 2),   # the Llama-3-8B shape (ring)
+])
 def test_draft_q_bounds(V, V_high, M):
     dev = need_cuda()
     logits = torch.from_numpy(np.random.default_rng(V).normal(0, 2, (M, V_high))
@@ -168,7 +172,7 @@ def test_draft_q_bounds(V, V_high, M):
     f2t_h = np.full(V, -1, np.int32)
     f2t_h[t2f_h] = np.arange(V_high, dtype=np.int32)
     q = Guarded((M, V), torch.float32, dev)
-    ws = Guarded((vt.workspace_bytes("q", M=M),), torch.uint8, dev)
+    ws = Guarded((vt.workspace_bytes("q", M=M),), torch.uint8, dev, fill=0)
     vt.draft_q(logits, torch.from_numpy(f2t_h).to(dev), V, temperature=0.9,
                out=q.t, ws=ws.t)
     q.check("q")
