@@ -77,7 +77,64 @@ struct TcArgs {
   float2* qstat;
   int nq;
   float inv_tau;
+  // 0: each CTA takes whole tiles (tile = blockIdx.x, blockIdx.x + grid, ...).
+  // 1: clusters of two CTAs per tile, rank r summing K stages
+  // [r * nkb / 2, (r + 1) * nkb / 2); each CTA sends the partner its partial
+  // sums of the partner's half of the rows through distributed shared memory
+  // and finishes its own half (rank 0 rows 0-63, rank 1 rows 64-127).
+  int ksplit;
 };
+
+// ------------------------------------------------ thread-block clusters
+// This CTA's rank in its cluster.
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of every CTA of the cluster arrives and waits (release /
+// acquire at cluster scope): shared-memory set-up before it is visible to
+// the other CTAs, and no CTA leaves while another may still access its
+// shared memory.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The address, in the cluster's shared window, of this CTA's shared
+// variable at `smem_addr` as seen in the CTA of rank `rank`.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t rank) {
+  uint32_t d;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(smem_addr), "r"(rank));
+  return d;
+}
+
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+// Arrive on an mbarrier of another CTA of the cluster, releasing this
+// thread's earlier writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t remote_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
+               : "memory");
+}
+
+// try_wait with acquire at cluster scope (the arrivals came from another CTA).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(tc::smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+
 
 __device__ __forceinline__ void record_error(unsigned* err, volatile int* abort) {
   *abort = 1;
@@ -159,6 +216,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int ntiles = (a.V_high + kTcTileRows - 1) / kTcTileRows;
   const int natoms = (a.d + kTcBlockK - 1) / kTcBlockK;  // K atoms in all
   const int nkb = (natoms + A - 1) / A;                   // stages per tile
+  // this CTA's tiles and K stages
+  const uint32_t rank = a.ksplit ? cluster_rank() : 0u;
+  const int tile0 = a.ksplit ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int tstep = a.ksplit ? ntiles : (int)gridDim.x;
+  const int kb_lo = a.ksplit ? (int)rank * nkb / 2 : 0;
+  const int kb_hi = a.ksplit ? ((int)rank + 1) * nkb / 2 : nkb;
+  // K split: the partner's partial sums of this CTA's rows land in xbuf,
+  // [N][64] fp32 after the stages, and xfull completes when all 128 of the
+  // partner's sending threads have arrived
+  __shared__ __align__(8) uint64_t xfull;
+  float* xbuf = reinterpret_cast<float*>(smem + (size_t)S * stage_bytes);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -170,6 +238,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc::mbar_init(&tempty[b], kTcEpilogueWarps);
     }
     tc::mbar_init(&drain, 1);
+    tc::mbar_init(&xfull, 128);
     abort_flag = 0;
     tc::fence_barrier_init();
   }
@@ -177,6 +246,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
+  if (a.ksplit) cluster_sync();  // the partner's xfull exists before any arrival
   const uint32_t tmem = tmem_base;
   // the per-row kernel (a programmatic dependent) may become resident now;
   // it waits for this grid's completion before reading the logits
@@ -186,12 +256,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // that ends, the producer only asks L2 for the first k-blocks of this
   // CTA's first W_high tile (weights; the TMA loads that use them come after
   // the wait).  Nothing else is read, and no logit written, before it.
-  if (warp == 0 && lane == 0 && (int)blockIdx.x < ntiles) {
+  if (warp == 0 && lane == 0 && tile0 < ntiles) {
     tc::prefetch_tensormap(&tmW);
     tc::prefetch_tensormap(&tmH);
-    const int npre = min(natoms, kTcPrefetchKBlocks);
-    for (int kb = 0; kb < npre; ++kb)
-      tc::tma_prefetch_l2_2d(&tmW, kb * kTcBlockK, (int)blockIdx.x * kTcTileRows);
+    const int x1 = min(min(natoms, kb_hi * A), kb_lo * A + kTcPrefetchKBlocks);
+    for (int x = kb_lo * A; x < x1; ++x)
+      tc::tma_prefetch_l2_2d(&tmW, x * kTcBlockK, tile0 * kTcTileRows);
   }
   grid_dependency_wait();
 
@@ -201,8 +271,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint32_t ph = 0;
       int issued = 0;  // loads issued, for the drain on abort
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
-        for (int kb = 0; kb < nkb; ++kb) {
+      for (int tile = tile0; ok && tile < ntiles; tile += tstep) {
+        for (int kb = kb_lo; kb < kb_hi; ++kb) {
           if (!wait_or_abort(&empty[s], ph ^ 1u, &abort_flag)) {
             ok = false;
             break;
@@ -239,13 +309,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int s = 0, it = 0;
       uint32_t ph = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++it) {
+      for (int tile = tile0; ok && tile < ntiles; tile += tstep, ++it) {
         const int acc = it & 1;
         const uint32_t aph = (uint32_t)(it >> 1) & 1u;
         if (!wait_or_abort(&tempty[acc], aph ^ 1u, &abort_flag)) { ok = false; break; }
         tc::tc_fence_after();
         const uint32_t d_tmem = tmem + (uint32_t)(acc * a.NB);
-        for (int kb = 0; kb < nkb; ++kb) {
+        for (int kb = kb_lo; kb < kb_hi; ++kb) {
           if (!wait_or_abort(&full[s], ph, &abort_flag)) { ok = false; break; }
           tc::tc_fence_after();
           const uint32_t a_base = tc::smem_u32(smem + (size_t)s * stage_bytes);
@@ -257,7 +327,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               tc::mma_bf16(d_tmem,
                            tc::sdesc_k_sw128(a_base + x * kTcABytes + 32 * j),
                            tc::sdesc_k_sw128(b_base + x * b_bytes + 32 * j), idesc,
-                           (kb > 0 || x > 0 || j > 0) ? 1u : 0u);
+                           (kb > kb_lo || x > 0 || j > 0) ? 1u : 0u);
           tc::mma_commit(&empty[s]);  // stage reusable once these complete
           if (++s == S) { s = 0; ph ^= 1u; }
         }
@@ -274,8 +344,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else {  // --------------------------------------------- epilogue warps
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     const int half = (warp - 2) >> 2;  // which chunks of the accumulator
+    // K split: the partner finishes the rows of this warp's quadrant (send)
+    // or this CTA does and adds the partner's part (receive)
+    const bool send = a.ksplit && (uint32_t)(q >> 1) != rank;
+    const bool recv = a.ksplit && !send;
+    const int xrow = 32 * (q & 1) + lane;  // the row within a CTA's half
     int it = 0;
-    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
+    for (int tile = tile0; tile < ntiles; tile += tstep, ++it) {
       const int acc = it & 1;
       const uint32_t aph = (uint32_t)(it >> 1) & 1u;
       if (!wait_or_abort(&tfull[acc], aph, &abort_flag)) {
@@ -283,14 +358,44 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         break;
       }
       tc::tc_fence_after();
+      const uint32_t tacc = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * a.NB);
+      if (send) {
+        const uint32_t xb = map_to_rank(tc::smem_u32(xbuf), rank ^ 1u);
+        for (int c0 = 32 * half; c0 < a.N; c0 += 64) {
+          float r[32];
+          tc::tmem_ld_32x32(tacc + (uint32_t)c0, r);
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (c0 + j < a.M) st_cluster_f32(xb + (uint32_t)(((c0 + j) * 64 + xrow) * 4), r[j]);
+        }
+        mbar_arrive_cluster(map_to_rank(tc::smem_u32(&xfull), rank ^ 1u));
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&tempty[acc]);
+        continue;
+      }
+      if (recv) {  // the partner's part of these rows (bounded wait)
+        bool ok = mbar_try_wait_cluster(&xfull, 0u);
+        const long long t0 = clock64();
+        while (!ok && !abort_flag && clock64() - t0 <= kWaitBudget)
+          ok = mbar_try_wait_cluster(&xfull, 0u);
+        if (!ok) {
+          if (lane == 0) record_error(a.err, &abort_flag);
+          break;
+        }
+      }
       const int row = tile * kTcTileRows + 32 * q + lane;
       const float b = row < a.V_high && a.bias ? __ldg(a.bias + row) : 0.f;
       for (int c0 = 32 * half; c0 < a.N; c0 += 64) {
         float r[32];
-        tc::tmem_ld_32x32(tmem + ((uint32_t)(32 * q) << 16) +
-                              (uint32_t)(acc * a.NB + c0),
-                          r);
+        tc::tmem_ld_32x32(tacc + (uint32_t)c0, r);
         tc::tmem_ld_wait();
+        if (recv) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (c0 + j < a.M) r[j] += xbuf[(c0 + j) * 64 + xrow];
+        }
 #pragma unroll
         for (int j = 0; j < 32; ++j) r[j] += b;
         if (row < a.V_high) {
@@ -311,6 +416,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, a.tmem_cols);
   }
+  // K split: neither CTA leaves while its partner may still write into its
+  // shared memory
+  if (a.ksplit) cluster_sync();
 }
 
 // ------------------------------------------------- per-row softmax + top-k
@@ -837,10 +945,17 @@ vt_status head_tc(const uint16_t* H, int M, int d, int64_t ldh,
   a.qstat = stats ? reinterpret_cast<float2*>(wsb + L.qstat) : nullptr;
   a.nq = quadrants(V_high);
   a.inv_tau = 1.0f / opt.tau;
+  // Few tiles (two per SM or fewer): split each tile's K stages between the
+  // two CTAs of a cluster, so twice as many SMs stream W_high; the exchange
+  // buffer of the partner's partial sums takes N * 64 * 4 bytes.
+  const int ntiles = (V_high + kTcTileRows - 1) / kTcTileRows;
+  const int natoms = (d + kTcBlockK - 1) / kTcBlockK;
+  a.ksplit = 2 * ntiles <= di.num_sms && natoms >= 2 * kTcMaxAtoms ? 1 : 0;
+  const int xbytes = a.ksplit ? a.N * 64 * 4 : 0;
   // K atoms per stage: the widest (up to kTcMaxAtoms) that still leaves
   // kTcMinStages stages in shared memory.
   const int atom_bytes = kTcABytes + a.N * kTcBlockK * 2;
-  const int fit = (di.max_smem_optin - 4096) / atom_bytes;  // atoms that fit
+  const int fit = (di.max_smem_optin - 4096 - xbytes) / atom_bytes;  // atoms that fit
   a.atoms = std::max(1, std::min(kTcMaxAtoms, fit / kTcMinStages));
   const int stage_bytes = a.atoms * atom_bytes;
   a.stages = std::min<int>(kTcMaxStages, fit / a.atoms);
@@ -850,12 +965,25 @@ vt_status head_tc(const uint16_t* H, int M, int d, int64_t ldh,
       !make_map(&tmH, H, (uint64_t)M, (uint64_t)d, (uint64_t)ldh, (uint32_t)a.N))
     return fail(VT_ERR_CUDA, "head_tc: cuTensorMapEncodeTiled failed");
   if (!allow_max_smem(head_tc_gemm_kernel, di)) return VT_ERR_CUDA;
-  const int ntiles = (V_high + kTcTileRows - 1) / kTcTileRows;
-  const int grid = std::min(ntiles, di.num_sms);
-  const int smem = a.stages * stage_bytes + 1024;
-  // a programmatic dependent of the work ahead of it in the stream
-  const cudaError_t e = launch_dependent(head_tc_gemm_kernel, dim3(grid),
-                                         dim3(kTcThreads), smem, s, tmW, tmH, a);
+  const int grid = a.ksplit ? 2 * ntiles : std::min(ntiles, di.num_sms);
+  const int smem = a.stages * stage_bytes + xbytes + 1024;
+  // a programmatic dependent of the work ahead of it in the stream; with the
+  // K split, in clusters of two CTAs
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.ksplit ? 2 : 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, head_tc_gemm_kernel, tmW, tmH, a);
   if (e != cudaSuccess)
     return fail(VT_ERR_CUDA, std::string("head_tc_gemm_kernel: ") + cudaGetErrorString(e));
   vt_status st = launch_status("head_tc_gemm_kernel");
