@@ -43,7 +43,9 @@ def test_bounded_wait_gives_up_and_reports():
     ids1, probs1 = vt.draft_head(H, W, None, 8)
     torch.cuda.synchronize()
     assert torch.equal(ids0, ids1)
-    assert torch.equal(probs0, probs1)
+    # (the GEMV deals its last rows dynamically, so the softmax sums may
+    # differ in the last bits from call to call)
+    assert (probs0 - probs1).abs().max().item() <= 1e-6
 
 
 def plant_timeout(lib, addr):
