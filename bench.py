@@ -57,7 +57,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweeps", action="store_true",
                     help="skip the tree-draft and batch sweeps")
-    ap.add_argument("--case", choices=["head", "count", "select", "gather"],
+    ap.add_argument("--case", choices=["head", "count", "select", "gather", "q"],
                     help="run one small case a few times (for profilers) and "
                          "exit")
     ap.add_argument("--M", type=int, default=1)
@@ -680,6 +680,15 @@ def run_case(args):
         for _ in range(args.calls):
             counts, _ = vt.count_tokens(tokens, 128256)
             vt.select_vocab(counts, args.V_high)
+    elif args.case == "q":
+        V = 128256
+        t2f = synth.expected_rank_ids(V, args.V_high, 1002).to(dev)
+        f2t = torch.full((V,), -1, dtype=torch.int32, device=dev)
+        f2t[t2f.long()] = torch.arange(args.V_high, dtype=torch.int32, device=dev)
+        lg = torch.randn(args.M, args.V_high, device=dev)
+        q = torch.empty(args.M, V, device=dev)
+        for _ in range(args.calls):
+            vt.draft_q(lg, f2t, V, out=q)
     elif args.case == "gather":
         W = synth.normal_bf16((128256, args.d), 0.02, seed=5, device=dev)
         t2f = synth.expected_rank_ids(128256, args.V_high, 1005).to(dev)
