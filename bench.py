@@ -42,7 +42,7 @@ CSRC = os.path.join(ROOT, "frequency_ranked_drafter_gb300", "csrc")
 # the sources the M = 1 head kernel is built from
 HEAD_KERNEL_SRCS = [os.path.join(CSRC, f) for f in
                     ("head_gemv.cu", "head_common.cuh", "vt_common.cuh",
-                     "tc_ptx.cuh")]
+                     "tc_ptx.cuh", "vt_checks.cuh")]
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "head_gemv_llama8b_m1.md")
 
 

@@ -51,21 +51,28 @@ class HeadOptions(ctypes.Structure):
                 ("offset", ctypes.c_uint64)]
 
 
+def _checked() -> bool:
+    """VT_CHECKS=1 in the environment selects the bounds-checked debug build."""
+    return os.environ.get("VT_CHECKS", "") == "1"
+
+
 def library_path() -> str:
-    return _build.LIB_PATH
+    return _build.CHECKS_LIB_PATH if _checked() else _build.LIB_PATH
 
 
 def load(build_if_missing: bool = True):
-    """Load (building first if needed) the CUDA library; raises if absent."""
+    """Load (building first if needed) the CUDA library; raises if absent.
+    With VT_CHECKS=1 in the environment, the bounds-checked debug build."""
     global _lib
     with _lock:
         if _lib is not None:
             return _lib
-        path = _build.LIB_PATH
-        if not os.path.exists(path) or not _build.up_to_date():
+        checks = _checked()
+        path = library_path()
+        if not os.path.exists(path) or not _build.up_to_date(checks):
             if not build_if_missing:
                 raise RuntimeError(f"CUDA library not built: {path}")
-            _build.build()
+            _build.build(checks=checks)
         lib = ctypes.CDLL(path)
         p, i32, i64, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
                            ctypes.c_size_t)
@@ -73,6 +80,8 @@ def load(build_if_missing: bool = True):
             "vt_status_string": ([ctypes.c_int], ctypes.c_char_p),
             "vt_last_error": ([], ctypes.c_char_p),
             "vt_version": ([], ctypes.c_int),
+            "vt_debug_build": ([], ctypes.c_int),
+            "vt_debug_checks": ([], ctypes.c_int),
             "vt_count_tokens_workspace_size": ([i32], sz),
             "vt_count_tokens": ([p, i64, i32, p, p, p, sz, p], ctypes.c_int),
             "vt_select_vocab_workspace_size": ([i32], sz),
@@ -86,6 +95,7 @@ def load(build_if_missing: bool = True):
                                   ctypes.POINTER(HeadOptions), p, p, p, p, sz,
                                   p], ctypes.c_int),
             "vt_selftest_wait_timeout": ([p, i64, p], ctypes.c_int),
+            "vt_selftest_check": ([p, i32, p], ctypes.c_int),
             "vt_draft_noise": ([ctypes.c_uint64, ctypes.c_uint64, i32, p, i64,
                                 p, p], ctypes.c_int),
             "vt_draft_q_workspace_size": ([i32], sz),

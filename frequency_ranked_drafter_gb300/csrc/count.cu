@@ -22,6 +22,7 @@
 //     16-bit SIMD lanes) into the uint32 counts.
 //   * Vocabularies larger than the shared-memory byte budget are counted in
 //     several passes over id ranges (the stream is re-read per pass).
+#include "vt_checks.cuh"
 #include "vt_common.cuh"
 
 namespace vt {
@@ -66,6 +67,7 @@ __device__ __noinline__ void settle_wrap(uint32_t old, uint32_t word,
                                          uint32_t b0, uint32_t* counts,
                                          uint32_t Vr, WrapCache& wc) {
   const uint32_t base = word << 2;
+  if (!VT_CHECKED(base + b0 < Vr)) return;
   cache_add(wc, base + b0, 256u, counts);
   for (uint32_t b = b0 + 1; b < 4; ++b) {
     if (base + b >= Vr) break;  // padding byte: never counted, never reported
@@ -215,10 +217,11 @@ __global__ void __launch_bounds__(kCountThreads, 1)
   if (kMode == kPadded && threadIdx.x == 0) invalid += sm[Vr >> 2] & 0xffu;
 
   uint32_t* slab = slabs + (size_t)blockIdx.x * words_padded;
-  for (int w = threadIdx.x; w < words_padded; w += kCountThreads)
-    slab[w] = sm[w];
+  if (VT_CHECKED(blockIdx.x < kCountMaxCtas))
+    for (int w = threadIdx.x; w < words_padded; w += kCountThreads)
+      slab[w] = sm[w];
   for (int i = threadIdx.x; i < kCacheSlots; i += kCountThreads)
-    if (wc.tag[i] != kEmptyTag && wc.cnt[i] != 0u)
+    if (wc.tag[i] != kEmptyTag && wc.cnt[i] != 0u && VT_CHECKED(wc.tag[i] < Vr))
       atomicAdd(&counts_pass[wc.tag[i]], wc.cnt[i]);
 
   if (lo == 0 && n_invalid) {

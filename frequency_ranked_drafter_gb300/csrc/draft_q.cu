@@ -17,6 +17,7 @@
 // gathered from L2.  Both are bound by writing q (M * V * 4 bytes).
 #include <cmath>
 
+#include "vt_checks.cuh"
 #include "vt_common.cuh"
 
 namespace vt {
@@ -242,6 +243,7 @@ __global__ void __launch_bounds__(kRowQThreads, 1)
   const int m = blockIdx.y;
   const float* row = logits + (size_t)m * V_high;
   const int f_begin = blockIdx.x * span, f_end = min(V, f_begin + span);
+  if (!VT_CHECKED(f_begin < V)) return;  // the grid covers V exactly
   // this thread's f2t entries of the fill: the first step's are requested
   // before the row is staged, each next step's before the current one is
   // written (two steps of 16-byte loads in flight)

@@ -7,6 +7,7 @@
 #include <limits.h>
 
 #include "tc_ptx.cuh"
+#include "vt_checks.cuh"
 #include "vt_common.cuh"
 
 namespace vt {
@@ -474,7 +475,7 @@ __device__ void head_final_merge(const HeadArgs& a, int MR, int G, float* stage,
       const entry_key x = sc.surv[c];
       int rank = 0;
       for (int q = 0; q < S; ++q) rank += sc.surv[q] > x;
-      if (rank < k) {
+      if (rank < k && VT_CHECKED(m < MR)) {
         ids[rank] = key_id(x);
         const float sv = a.opt.sample ? sc.surv_s[c] : key_logit(x);
         probs[rank] = expf(sv - mg) / sg;

@@ -241,7 +241,11 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
   float* rec[MR];
 #pragma unroll
   for (int m = 0; m < MR; ++m) {
-    rec[m] = a.part + ((size_t)m * gridDim.x + blockIdx.x) * a.pstride;
+    // the workspace holds kHeadMaxCtas records per hidden state (a failed
+    // check in a debug build writes record 0 instead)
+    rec[m] = a.part + (VT_CHECKED(gridDim.x <= kHeadMaxCtas)
+                           ? ((size_t)m * gridDim.x + blockIdx.x) * a.pstride
+                           : 0);
     if (lane == 0) { w_mx[m][warp] = mx[m]; w_se[m][warp] = se[m]; }
   }
   int level = 0;

@@ -46,6 +46,7 @@ __global__ void sets_scatter_kernel(const int32_t* __restrict__ ids_g,
                                     float* __restrict__ out_probs) {
   for (int t = threadIdx.x; t < L.n * k; t += blockDim.x) {
     const int j = t / k, r = t - j * k;
+    if (!VT_CHECKED(L.rows[j] >= 0 && L.rows[j] < kSetsMaxRows)) continue;
     out_ids[(int64_t)L.rows[j] * k + r] = ids_g[t];
     out_probs[(int64_t)L.rows[j] * k + r] = probs_g[t];
   }

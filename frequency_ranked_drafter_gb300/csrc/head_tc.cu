@@ -194,7 +194,8 @@ __device__ __forceinline__ void quadrant_stats(const TcArgs& a, const float (&r)
     x[j] = sv[j] > -INFINITY ? __expf(sv[j] - mj) : 0.f;
   }
   const float se = warp_transpose_reduce(x, [](float p, float q) { return p + q; });
-  if (c0 + lane < a.M) a.qstat[(size_t)(c0 + lane) * a.nq + quad] = make_float2(mx, se);
+  if (c0 + lane < a.M && VT_CHECKED(quad < a.nq))
+    a.qstat[(size_t)(c0 + lane) * a.nq + quad] = make_float2(mx, se);
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -567,7 +568,7 @@ __global__ void __launch_bounds__(kRowThreads, 4)
     }
   }
   __syncthreads();
-  float* mypart = a.part + ((size_t)m * a.P + part_idx) * ps;
+  float* mypart = a.part + ((size_t)m * a.P + (VT_CHECKED(part_idx < a.P) ? part_idx : 0)) * ps;
   const int S = min(s_cnt, kRowSurvivors);
   // slots this CTA cannot fill stay (-inf, INT_MAX)
   for (int r = tid; r < k; r += kRowThreads) {

@@ -23,6 +23,7 @@
 //     writes VT_ERR_TIMEOUT to the workspace error word;
 //   * the last pass writes t2f, f2t and the two sums instead of a copy.
 // About 1 MB of data at V = 128256: the cost is latency, not bandwidth.
+#include "vt_checks.cuh"
 #include "vt_common.cuh"
 
 namespace vt {
@@ -197,14 +198,16 @@ __global__ void __launch_bounds__(kSelThreads, 1) onesweep_kernel(PassArgs a) {
     const uint32_t pos = dstart[dig] + base[dig] + wcnt[warp][dig] + rk;
     if (a.final_pass) {
       if ((int)pos < a.V_high) {
-        a.t2f[pos] = val;
-        a.f2t[val] = (int32_t)pos;
+        if (VT_CHECKED(val >= 0 && val < a.V)) {
+          a.t2f[pos] = val;
+          a.f2t[val] = (int32_t)pos;
+        }
         kept = key;
-      } else {
+      } else if (VT_CHECKED(val >= 0 && val < a.V)) {
         a.f2t[val] = -1;
       }
       total = key;
-    } else {
+    } else if (VT_CHECKED(pos < (uint32_t)a.V)) {
       a.keys_out[pos] = key;
       a.vals_out[pos] = val;
     }

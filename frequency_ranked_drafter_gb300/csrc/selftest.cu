@@ -7,7 +7,8 @@
 // tc::mbar_wait with a cycle budget; on expiry the kernel records
 // VT_ERR_TIMEOUT in the workspace error word and stops.  Here one CTA
 // initialises an mbarrier on which nothing ever arrives and waits on it with
-// the caller's budget.  The pages have no counterpart.
+// the caller's budget.  vt_selftest_check does the same for the debug
+// build's bounds checks.  The pages have no counterpart.
 #include "head_common.cuh"
 
 namespace vt {
@@ -26,8 +27,26 @@ __global__ void __launch_bounds__(32)
     atomicExch(err, (unsigned)VT_ERR_TIMEOUT);
 }
 
+// buf[i] = i for i = 0 .. n, each write guarded by a check that allows
+// only i < n: every write lands inside buf (n + 1 values) in either build,
+// and in a bounds-checked build the last one is skipped and reported.
+__global__ void check_selftest_kernel(uint32_t* buf, int n) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i <= n;
+       i += gridDim.x * blockDim.x)
+    if (VT_CHECKED(i < n)) buf[i] = (uint32_t)i;
+}
+
 }  // namespace
 }  // namespace vt
+
+extern "C" vt_status vt_selftest_check(uint32_t* buf, int32_t n, void* stream) {
+  using namespace vt;
+  if (!buf || !aligned(buf, 4) || n < 1 || n > (1 << 30))
+    return fail(VT_ERR_INVALID_ARG, "vt_selftest_check: need buf and 1 <= n <= 2^30");
+  const int blocks = (int)std::min<int64_t>(((int64_t)n + 256) / 256, 1024);
+  check_selftest_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>(buf, n);
+  return launch_status("check_selftest_kernel");
+}
 
 extern "C" vt_status vt_selftest_wait_timeout(uint32_t* err_word,
                                               int64_t budget_cycles,

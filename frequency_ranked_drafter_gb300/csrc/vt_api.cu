@@ -4,9 +4,22 @@
 #include <string>
 #include <utility>
 
+#include <vector>
+
 #include "vt_common.cuh"
 
 namespace vt {
+
+// Readers of the translation units' check words (debug builds only; each
+// unit registers at load time).
+static std::vector<unsigned (*)()>& check_readers() {
+  static std::vector<unsigned (*)()> readers;
+  return readers;
+}
+
+void register_check_word(unsigned (*read_and_clear)()) {
+  check_readers().push_back(read_and_clear);
+}
 
 static thread_local std::string g_last_error;
 
@@ -94,6 +107,24 @@ const char* vt_status_string(int status) {
 const char* vt_last_error(void) { return vt::g_last_error.c_str(); }
 
 int vt_version(void) { return 101; }
+
+int vt_debug_build(void) {
+#ifdef VT_CHECKS
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+int vt_debug_checks(void) {
+  int first = 0;
+  for (auto read : vt::check_readers()) {
+    const unsigned v = read();
+    if (v == ~0u) return -1;
+    if (v && !first) first = (int)v;
+  }
+  return first;
+}
 
 size_t vt_workspace_size(int32_t op, int32_t M, int32_t n, int32_t k) {
   switch (op) {

@@ -74,6 +74,33 @@ const char* vt_last_error(void);
 int vt_version(void);
 
 /* ------------------------------------------------------------------------
+ * Debug builds.  The library can be compiled with VT_CHECKS defined (the
+ * build script's checked variant, libvt_gb300_checks.so): every kernel then
+ * tests the indices of its index-computed global accesses, skips an access
+ * that would fall outside its buffer and records the source line of the
+ * first such check.  Nothing traps.  The release build has no checks.
+ *
+ *   vt_debug_build   1 in a checked build, 0 otherwise.
+ *   vt_debug_checks  after the work has finished (it reads device memory
+ *                    synchronously): 0 if no check failed since the last
+ *                    call, else the source line of a failed check (then
+ *                    cleared); -1 if the words could not be read.  Always 0
+ *                    in a release build.
+ * ------------------------------------------------------------------------ */
+int vt_debug_build(void);
+int vt_debug_checks(void);
+
+/* vt_selftest_check — one kernel whose bounds check fails by design, to see
+ * the debug build's reporting work: it writes buf[i] = i for i = 0 .. n with
+ * each write guarded by a check that allows only i < n.  buf (device,
+ * uint32[n + 1], 4-byte aligned) holds every index, so nothing lands outside
+ * it in either build; a release build writes all n + 1 values, a checked
+ * build skips buf[n] and vt_debug_checks() then reports the check's line.
+ * 1 <= n <= 2^30.  Argument errors return VT_ERR_INVALID_ARG with nothing
+ * launched. */
+vt_status vt_selftest_check(uint32_t* buf, int32_t n, void* stream);
+
+/* ------------------------------------------------------------------------
  * vt_workspace_size — workspace bytes of one operation, in one call; the
  * same numbers as the per-operation *_workspace_size functions below.
  *

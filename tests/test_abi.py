@@ -40,6 +40,26 @@ def test_library_exports_every_declared_symbol(lib):
     assert not missing, missing
 
 
+def test_release_build_has_no_checks(lib):
+    assert lib.vt_debug_build() == 0
+    assert lib.vt_debug_checks() == 0  # no check words: no device access
+    assert lib.vt_selftest_check(None, 10, None) == INVALID
+    assert lib.vt_selftest_check(FAKE, 0, None) == INVALID
+    assert lib.vt_selftest_check(FAKE + 2, 10, None) == INVALID
+
+
+def test_checked_build_compiles_and_exports_the_same_symbols():
+    """The bounds-checked variant (-DVT_CHECKS) builds, says so, and exports
+    every function vt.h declares."""
+    from frequency_ranked_drafter_gb300 import build as vt_build
+    path = vt_build.build(checks=True)
+    raw = ctypes.CDLL(path)
+    missing = [n for n in declared_functions() if not hasattr(raw, n)]
+    assert not missing, missing
+    raw.vt_debug_build.restype = ctypes.c_int
+    assert raw.vt_debug_build() == 1
+
+
 def test_status_strings_and_version(lib):
     assert lib.vt_status_string(0) == b"VT_OK"
     assert lib.vt_status_string(1) == b"VT_ERR_INVALID_ARG"
