@@ -168,7 +168,8 @@ __global__ void __launch_bounds__(kFillThreads)
 // exp(s - max) from shared memory in a second pass (no branch and one
 // exponential per value, where an online fold needed a compare and up to
 // two), then fills its 1/P of q[m], the kept values gathered from shared
-// memory (no L2 sector per gathered value), q in 16-byte stores.
+// memory (no L2 sector per gathered value), f2t loads and q stores both
+// 512 contiguous bytes per warp instruction.
 // Exponentials use the fast hardware form (relative error about 1e-6 here,
 // far inside the 1e-4 bound on q).
 constexpr int kRowQThreads = 1024;
@@ -241,47 +242,56 @@ __global__ void __launch_bounds__(kRowQThreads, 1)
                  float* __restrict__ q, int span, bool vec) {
   extern __shared__ __align__(16) float srow[];  // [V_high] logit / T
   const int m = blockIdx.y;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const float* row = logits + (size_t)m * V_high;
   const int f_begin = blockIdx.x * span, f_end = min(V, f_begin + span);
   if (!VT_CHECKED(f_begin < V)) return;  // the grid covers V exactly
-  // this thread's f2t entries of the fill: the first step's are requested
-  // before the row is staged, each next step's before the current one is
-  // written (two steps of 16-byte loads in flight)
-  auto load_idx = [&](int f0, int (&idx)[kFillIds]) {
-    if (vec && f2t && f0 + kFillIds <= f_end) {
-      const int4 a = __ldg(reinterpret_cast<const int4*>(f2t + f0));
-      const int4 b = __ldg(reinterpret_cast<const int4*>(f2t + f0) + 1);
-      idx[0] = a.x; idx[1] = a.y; idx[2] = a.z; idx[3] = a.w;
-      idx[4] = b.x; idx[5] = b.y; idx[6] = b.z; idx[7] = b.w;
-    } else {
+  // A warp's step covers 32 * kFillIds consecutive ids; lane l takes the
+  // four-id chunks at 4 l and 4 l + 128, so every f2t load and q store of
+  // the warp is 512 contiguous bytes.  The first step's f2t entries are
+  // requested before the row is staged, each next step's before the current
+  // one is written.
+  static_assert(kFillIds == 8, "two chunks of four ids per lane");
+  auto load_idx = [&](int fw, int (&idx)[kFillIds]) {
 #pragma unroll
-      for (int j = 0; j < kFillIds; ++j)
-        idx[j] = f0 + j < f_end ? (f2t ? __ldg(f2t + f0 + j) : f0 + j) : -1;
+    for (int v = 0; v < 2; ++v) {
+      const int f = fw + 128 * v + 4 * lane;
+      if (vec && f2t && f + 4 <= f_end) {
+        const int4 x = __ldg(reinterpret_cast<const int4*>(f2t + f));
+        idx[4 * v] = x.x; idx[4 * v + 1] = x.y; idx[4 * v + 2] = x.z; idx[4 * v + 3] = x.w;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          idx[4 * v + j] = f + j < f_end ? (f2t ? __ldg(f2t + f + j) : f + j) : -1;
+      }
     }
   };
   constexpr int kStep = kRowQThreads * kFillIds;
   int idx[kFillIds];
-  int f0 = f_begin + threadIdx.x * kFillIds;
-  if (f0 < f_end) load_idx(f0, idx);
+  int fw = f_begin + warp * 32 * kFillIds;
+  if (fw < f_end) load_idx(fw, idx);
   const float2 st = stage_row_stats(row, V_high, inv_tau, srow);
   const float mx = st.x, inv_sum = st.y;
   float* qm = q + (size_t)m * V;
-  for (; f0 < f_end; f0 += kStep) {
+  for (; fw < f_end; fw += kStep) {
     int nidx[kFillIds];
-    if (f0 + kStep < f_end) load_idx(f0 + kStep, nidx);
-    const bool full = vec && f0 + kFillIds <= f_end;
-    float o[kFillIds];
+    if (fw + kStep < f_end) load_idx(fw + kStep, nidx);
 #pragma unroll
-    for (int j = 0; j < kFillIds; ++j)
-      o[j] = (unsigned)idx[j] < (unsigned)V_high ? __expf(srow[idx[j]] - mx) * inv_sum : 0.f;
-    if (full) {
-      float4* dst = reinterpret_cast<float4*>(qm + f0);
-      dst[0] = make_float4(o[0], o[1], o[2], o[3]);
-      dst[1] = make_float4(o[4], o[5], o[6], o[7]);
-    } else {
+    for (int v = 0; v < 2; ++v) {
+      const int f = fw + 128 * v + 4 * lane;
+      float o[4];
 #pragma unroll
-      for (int j = 0; j < kFillIds; ++j)
-        if (f0 + j < f_end) qm[f0 + j] = o[j];
+      for (int j = 0; j < 4; ++j) {
+        const int ix = idx[4 * v + j];
+        o[j] = (unsigned)ix < (unsigned)V_high ? __expf(srow[ix] - mx) * inv_sum : 0.f;
+      }
+      if (vec && f + 4 <= f_end) {
+        *reinterpret_cast<float4*>(qm + f) = make_float4(o[0], o[1], o[2], o[3]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (f + j < f_end) qm[f + j] = o[j];
+      }
     }
 #pragma unroll
     for (int j = 0; j < kFillIds; ++j) idx[j] = nidx[j];
