@@ -106,7 +106,7 @@ const char* vt_status_string(int status) {
 
 const char* vt_last_error(void) { return vt::g_last_error.c_str(); }
 
-int vt_version(void) { return 101; }
+int vt_version(void) { return 102; }
 
 int vt_debug_build(void) {
 #ifdef VT_CHECKS

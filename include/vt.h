@@ -42,7 +42,9 @@
  *     workspace and the kernel returns; the call's outputs are then
  *     incomplete.  The call itself has returned VT_OK by then (it is
  *     asynchronous): read the word after synchronising the stream.
- *     vt_host_step_run reads it for you and returns VT_ERR_TIMEOUT.
+ *     vt_host_step_run reads it for you and returns VT_ERR_TIMEOUT.  After a
+ *     timeout the head's counters may be left set: zero-fill its workspace
+ *     again before the next call.
  */
 #ifndef VT_H_
 #define VT_H_
