@@ -134,13 +134,14 @@ _ERR_WORD = 128  # byte offset of the device error word in every workspace
 
 def check_error_word(fn: str, ws: torch.Tensor):
     """Reads the device error word of a call's workspace (synchronising
-    with the workspace's device), writes 0 back if it was set and raises
+    with the workspace's device); if it was set, zero-fills the workspace
+    (the word, and any counters the interrupted call left set) and raises
     VTError(VT_ERR_TIMEOUT): a bounded wait inside that call's kernels gave
     up, and its outputs are incomplete."""
     word = ws[_ERR_WORD:_ERR_WORD + 4].view(torch.int32)
     e = int(word.item())
     if e != 0:
-        word.zero_()
+        ws.zero_()
         raise VTError(fn, e, "a bounded wait inside the kernels gave up; "
                              "the call's outputs are incomplete")
 
