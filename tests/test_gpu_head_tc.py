@@ -59,6 +59,21 @@ def test_tc_shapes(d, V_high, M, k):
     run_tc(d, V_high, M, k, seed=d + V_high + M)
 
 
+@pytest.mark.parametrize("d,V_high,M,k", [
+    (520, 1000, 9, 10),      # 9 K atoms, 3 stages: halves of 1 and 2 stages
+    (1000, 4000, 20, 7),     # ragged last K atom (1000 = 15 x 64 + 40)
+    (4096, 9728, 60, 10),    # 76 tiles on 152 SMs: the largest split grid
+    (2056, 257, 64, 32),     # one full tile and one row, N = 64
+    (8200, 640, 3, 4),       # long K, N = 16
+])
+def test_tc_k_split_between_cluster_pairs(d, V_high, M, k):
+    """With at most half as many 128-row tiles as SMs (and at least eight K
+    atoms), the two CTAs of a cluster each sum half of a tile's K stages and
+    exchange partial sums through distributed shared memory; every logit and
+    the top-k against the oracle, odd stage counts and ragged K included."""
+    run_tc(d, V_high, M, k, seed=d + V_high + M)
+
+
 def test_tc_identity_map():
     run_tc(1024, 5000, 24, 10, seed=3, use_t2f=False)
 
