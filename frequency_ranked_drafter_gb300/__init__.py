@@ -25,7 +25,8 @@ from . import build as _build
 
 __all__ = ["VTError", "load", "library_path", "count_tokens", "select_vocab",
            "gather_rows", "draft_head", "draft_head_host", "build_vocab",
-           "coverage", "Workspace", "workspace_bytes", "check_error_word"]
+           "coverage", "Workspace", "workspace_bytes", "check_error_word",
+           "save_vocab", "load_vocab"]
 
 VT_OK = 0
 _STATUS = {0: "VT_OK", 1: "VT_ERR_INVALID_ARG", 2: "VT_ERR_CUDA",
@@ -545,4 +546,45 @@ def build_vocab(tokens: torch.Tensor, V: int, V_high: int,
         out["W_high"] = gather_rows(W, t2f)
     if b is not None:
         out["b_high"] = gather_bias(b, t2f)
+    return out
+
+
+_VOCAB_FORMAT = 1
+
+
+def save_vocab(path: str, vocab: dict) -> None:
+    """Writes the offline build's result (the output of ``build_vocab``:
+    counts, t2f, f2t, sums and n_invalid; not W_high, which is rebuilt from
+    the model's weights with ``gather_rows``) to a ``.npz`` file, so a
+    serving process can load the kept vocabulary instead of recounting the
+    corpus."""
+    import numpy as np
+    arrays = {"format": np.array([_VOCAB_FORMAT], dtype=np.int64)}
+    for key in ("counts", "t2f", "f2t", "sums", "n_invalid"):
+        t = vocab[key].detach().cpu()
+        if t.dtype == torch.uint32:
+            t = t.view(torch.int32)  # stored as raw 32-bit words
+        arrays[key] = t.numpy()
+    np.savez(path, **arrays)
+
+
+def load_vocab(path: str, device: torch.device | str = "cuda") -> dict:
+    """Reads a file written by ``save_vocab``; returns the same tensors
+    (counts uint32[V], t2f int32[V_high], f2t int32[V], sums int64[2],
+    n_invalid int64[1]) on ``device``, checked for consistency: t2f and f2t
+    are inverse maps over the kept ids and V_high <= V."""
+    import numpy as np
+    with np.load(path) as z:
+        if int(z["format"][0]) != _VOCAB_FORMAT:
+            raise ValueError(f"{path}: unknown vocabulary file format")
+        arr = {k: z[k] for k in ("counts", "t2f", "f2t", "sums", "n_invalid")}
+    t2f, f2t = arr["t2f"], arr["f2t"]
+    V, V_high = f2t.size, t2f.size
+    if (arr["counts"].size != V or V_high > V or t2f.min(initial=0) < 0
+            or t2f.max(initial=0) >= V
+            or not np.array_equal(f2t[t2f], np.arange(V_high))
+            or int((f2t >= 0).sum()) != V_high):
+        raise ValueError(f"{path}: maps are not consistent")
+    out = {k: torch.from_numpy(v).to(device) for k, v in arr.items()}
+    out["counts"] = out["counts"].view(torch.uint32)
     return out
