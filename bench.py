@@ -260,7 +260,9 @@ def hold_stream(torch, us: float = 200.0):
     device-side spin) so that the work launched right after it is queued
     before the device reaches the start event: the timed region then holds
     device time only, not the host's graph-launch latency."""
-    torch.cuda._sleep(int(us * 2000))  # ~2 GHz SM clock
+    sleep = getattr(torch.cuda, "_sleep", None)
+    if sleep is not None:
+        sleep(int(us * 2000))  # ~2 GHz SM clock
 
 
 def graph_seconds(torch, fn, n: int, reps: int = 20):
