@@ -3,9 +3,9 @@
 Every kernel of that build tests the indices of its index-computed global
 accesses, skips an access that would leave its buffer and records the
 source line.  Here: the reporting path works (a kernel whose check fails by
-design, inside an in-bounds buffer), and the parity suites of the head and
-the canary bounds tests pass under the checked build with no failed check
-(conftest asserts that after every GPU test when VT_CHECKS=1)."""
+design, inside an in-bounds buffer), and every GPU test (parity, canaries,
+error words) passes under the checked build with no failed check (conftest
+asserts that after every GPU test when VT_CHECKS=1)."""
 import os
 import subprocess
 import sys
@@ -51,11 +51,7 @@ def test_suites_pass_under_the_checked_build():
     env = dict(os.environ, VT_CHECKS="1")
     r = subprocess.run(
         [sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu",
-         "-p", "no:cacheprovider",
-         os.path.join(ROOT, "tests", "test_gpu_debug_build.py"),
-         os.path.join(ROOT, "tests", "test_gpu_canary.py"),
-         os.path.join(ROOT, "tests", "test_gpu_head_tc.py"),
-         os.path.join(ROOT, "tests", "test_gpu_build.py")],
+         "-p", "no:cacheprovider", os.path.join(ROOT, "tests")],
         env=env, cwd=ROOT, capture_output=True, text=True, timeout=1800)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
     assert " passed" in r.stdout
