@@ -16,11 +16,12 @@
 // swizzle) of the W tile and of H into a ring of shared-memory stages with
 // TMA (a stage is up to four such K blocks of the same rows, requested back
 // to back); one thread of warp 1 issues tcgen05.mma into a double-buffered TMEM
-// accumulator; warps 2-9 read finished accumulators out of TMEM (two warps
-// per 32-lane quadrant, alternate 32-column chunks, so the last tile's
-// epilogue, which nothing overlaps, takes half as long) and store fp32
-// logits (tile rows along lanes, so every store is a coalesced 128-byte row
-// segment).  At these M the work stays bound by the W_high stream.
+// accumulator; warps 2-17 read finished accumulators out of TMEM (four warps
+// per 32-lane quadrant, each every fourth 16-column chunk, so the last
+// tile's epilogue, which nothing overlaps, is spread over all sixteen) and
+// store fp32 logits (tile rows along lanes, so every store is a coalesced
+// 128-byte row segment).  At these M the work stays bound by the W_high
+// stream.
 //
 // Softmax + top-k: each hidden state's V_high logits (L2-resident, bias
 // added by the GEMM epilogue) are split over CTAs of 4096; each CTA reduces
@@ -44,10 +45,14 @@
 namespace vt {
 namespace {
 
-// warp 0 TMA, warp 1 MMA + TMEM, warps 2-9 epilogue (two warps per TMEM lane
-// quadrant, each taking every other 32-column chunk of the accumulator)
-constexpr int kTcThreads = 320;
-constexpr int kTcEpilogueWarps = 8;
+// warp 0 TMA, warp 1 MMA + TMEM, warps 2-17 epilogue (four warps per TMEM
+// lane quadrant, each taking every fourth 16-column chunk of the
+// accumulator).  The last tile's epilogue is exposed: with 8 warps and
+// 32-column chunks it took ~2 us at N = 64, most of it the quadrant
+// statistics' shuffles and exponentials of one chunk per warp.
+constexpr int kTcThreads = 576;
+constexpr int kTcEpilogueWarps = 16;
+constexpr int kTcChunk = 16;  // accumulator columns (hidden states) per chunk
 constexpr int kTcMaxStages = 6;
 // k-blocks of a CTA's first W_high tile prefetched into L2 before the
 // dependency wait.
@@ -136,6 +141,19 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
 
 
 
+// 16 consecutive 32-bit columns of this warp's 32 TMEM lanes (lane = row).
+__device__ __forceinline__ void tmem_ld_32x32_x16(uint32_t taddr, float (&r)[kTcChunk]) {
+  uint32_t* u = reinterpret_cast<uint32_t*>(r);
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]),
+        "=r"(u[6]), "=r"(u[7]), "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]),
+        "=r"(u[12]), "=r"(u[13]), "=r"(u[14]), "=r"(u[15])
+      : "r"(taddr)
+      : "memory");
+}
+
 __device__ __forceinline__ void record_error(unsigned* err, volatile int* abort) {
   *abort = 1;
   atomicExch(err, (unsigned)VT_ERR_TIMEOUT);
@@ -153,49 +171,53 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
   return true;
 }
 
-// Reduces, per column j of a 32-column accumulator chunk, the 32 values the
-// lanes of a warp hold (lane = row) with op, transposed: lane l returns the
-// result for column l.  31 shuffles: at each halving step a lane keeps one
-// half of its columns and takes its partner's share of that half.
-template <class Op>
-__device__ __forceinline__ float warp_transpose_reduce(float (&x)[32], Op op) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int h = 16; h >= 1; h >>= 1) {
-    const bool up = (lane & h) != 0;
-#pragma unroll
-    for (int i = 0; i < h; ++i) {
-      const float keep = up ? x[i + h] : x[i];
-      const float send = up ? x[i] : x[i + h];
-      x[i] = op(keep, __shfl_xor_sync(~0u, send, h));
-    }
-  }
-  return x[0];
+// Merges two (max, sum of exp(x - max)) pairs of the same hidden state:
+// (m1, s1) + (m2, s2) = (max, s_max + s_min * exp(min - max)), where s_max
+// belongs to the pair with the larger max.  An empty pair (-inf, 0) adds
+// nothing.
+__device__ __forceinline__ void merge_stat(float& m, float& s, float pm, float ps) {
+  const float hi = fmaxf(m, pm), lo = fminf(m, pm);
+  const float e = lo > -INFINITY ? __expf(lo - hi) : 0.f;
+  s = m >= pm ? fmaf(ps, e, s) : fmaf(s, e, ps);
+  m = hi;
 }
 
 // Softmax statistics of one 32-row quadrant of a tile for the chunk's
-// hidden states c0 .. c0+31: max of s = logit / T over the quadrant's rows
-// (rows past V_high excluded) and the sum of exp(s - max); lane l writes
-// hidden state c0 + l's pair.  The row kernel folds these into the softmax
-// normaliser and bounds the k-th best score from them.
-__device__ __forceinline__ void quadrant_stats(const TcArgs& a, const float (&r)[32],
+// hidden states c0 .. c0+15: max of s = logit / T over the quadrant's rows
+// (rows past V_high excluded) and the sum of exp(s - max).  Each lane
+// starts from its row's pairs (s, 1); the pairs are merged across lanes
+// along a transposed halving (at each step a lane keeps half of its hidden
+// states and merges its partner's pairs for that half, one shuffle pair and
+// one exponential per merge), so after four steps lane l holds hidden state
+// c0 + (l & 15) over its half-warp, and one more merge with lane l ^ 16
+// covers all 32 rows; lanes 0-15 write the pairs.  The row kernel folds
+// these into the softmax normaliser and bounds the k-th best score from
+// them.
+__device__ __forceinline__ void quadrant_stats(const TcArgs& a, const float (&r)[kTcChunk],
                                                int row, int c0, int quad) {
   const int lane = threadIdx.x & 31;
-  float sv[32], x[32];
+  const bool valid = row < a.V_high;
+  float m[kTcChunk], sm[kTcChunk];
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    sv[j] = row < a.V_high ? __fmul_rn(r[j], a.inv_tau) : -INFINITY;
-    x[j] = sv[j];
+  for (int j = 0; j < kTcChunk; ++j) {
+    m[j] = valid ? __fmul_rn(r[j], a.inv_tau) : -INFINITY;
+    sm[j] = valid ? 1.f : 0.f;
   }
-  const float mx = warp_transpose_reduce(x, [](float p, float q) { return fmaxf(p, q); });
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const float mj = __shfl_sync(~0u, mx, j);
-    x[j] = sv[j] > -INFINITY ? __expf(sv[j] - mj) : 0.f;
+  for (int h = kTcChunk / 2; h >= 1; h >>= 1) {
+    const bool up = (lane & h) != 0;
+#pragma unroll
+    for (int i = 0; i < h; ++i) {
+      float km = up ? m[i + h] : m[i], ks = up ? sm[i + h] : sm[i];
+      const float om = up ? m[i] : m[i + h], os = up ? sm[i] : sm[i + h];
+      merge_stat(km, ks, __shfl_xor_sync(~0u, om, h), __shfl_xor_sync(~0u, os, h));
+      m[i] = km;
+      sm[i] = ks;
+    }
   }
-  const float se = warp_transpose_reduce(x, [](float p, float q) { return p + q; });
-  if (c0 + lane < a.M && VT_CHECKED(quad < a.nq))
-    a.qstat[(size_t)(c0 + lane) * a.nq + quad] = make_float2(mx, se);
+  merge_stat(m[0], sm[0], __shfl_xor_sync(~0u, m[0], 16), __shfl_xor_sync(~0u, sm[0], 16));
+  if (lane < kTcChunk && c0 + lane < a.M && VT_CHECKED(quad < a.nq))
+    a.qstat[(size_t)(c0 + lane) * a.nq + quad] = make_float2(m[0], sm[0]);
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -224,7 +246,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int kb_lo = a.ksplit ? (int)rank * nkb / 2 : 0;
   const int kb_hi = a.ksplit ? ((int)rank + 1) * nkb / 2 : nkb;
   // K split: the partner's partial sums of this CTA's rows land in xbuf,
-  // [N][64] fp32 after the stages, and xfull completes when all 128 of the
+  // [N][64] fp32 after the stages, and xfull completes when all 256 of the
   // partner's sending threads have arrived
   __shared__ __align__(8) uint64_t xfull;
   float* xbuf = reinterpret_cast<float*>(smem + (size_t)S * stage_bytes);
@@ -239,7 +261,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc::mbar_init(&tempty[b], kTcEpilogueWarps);
     }
     tc::mbar_init(&drain, 1);
-    tc::mbar_init(&xfull, 128);
+    tc::mbar_init(&xfull, 32 * kTcEpilogueWarps / 2);
     abort_flag = 0;
     tc::fence_barrier_init();
   }
@@ -344,7 +366,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else {  // --------------------------------------------- epilogue warps
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
-    const int half = (warp - 2) >> 2;  // which chunks of the accumulator
+    const int part = (warp - 2) >> 2;  // which chunks of the accumulator
     // K split: the partner finishes the rows of this warp's quadrant (send)
     // or this CTA does and adds the partner's part (receive)
     const bool send = a.ksplit && (uint32_t)(q >> 1) != rank;
@@ -362,12 +384,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint32_t tacc = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * a.NB);
       if (send) {
         const uint32_t xb = map_to_rank(tc::smem_u32(xbuf), rank ^ 1u);
-        for (int c0 = 32 * half; c0 < a.N; c0 += 64) {
-          float r[32];
-          tc::tmem_ld_32x32(tacc + (uint32_t)c0, r);
+        for (int c0 = kTcChunk * part; c0 < a.N; c0 += 4 * kTcChunk) {
+          float r[kTcChunk];
+          tmem_ld_32x32_x16(tacc + (uint32_t)c0, r);
           tc::tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
+          for (int j = 0; j < kTcChunk; ++j)
             if (c0 + j < a.M) st_cluster_f32(xb + (uint32_t)(((c0 + j) * 64 + xrow) * 4), r[j]);
         }
         mbar_arrive_cluster(map_to_rank(tc::smem_u32(&xfull), rank ^ 1u));
@@ -388,20 +410,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       const int row = tile * kTcTileRows + 32 * q + lane;
       const float b = row < a.V_high && a.bias ? __ldg(a.bias + row) : 0.f;
-      for (int c0 = 32 * half; c0 < a.N; c0 += 64) {
-        float r[32];
-        tc::tmem_ld_32x32(tacc + (uint32_t)c0, r);
+      for (int c0 = kTcChunk * part; c0 < a.N; c0 += 4 * kTcChunk) {
+        float r[kTcChunk];
+        tmem_ld_32x32_x16(tacc + (uint32_t)c0, r);
         tc::tmem_ld_wait();
         if (recv) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
+          for (int j = 0; j < kTcChunk; ++j)
             if (c0 + j < a.M) r[j] += xbuf[(c0 + j) * 64 + xrow];
         }
 #pragma unroll
-        for (int j = 0; j < 32; ++j) r[j] += b;
+        for (int j = 0; j < kTcChunk; ++j) r[j] += b;
         if (row < a.V_high) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
+          for (int j = 0; j < kTcChunk; ++j)
             if (c0 + j < a.M) a.logits[(size_t)(c0 + j) * a.V_high + row] = r[j];
         }
         if (a.qstat) quadrant_stats(a, r, row, c0, tile * 4 + q);
