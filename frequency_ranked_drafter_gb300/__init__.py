@@ -480,10 +480,10 @@ class HostDraftHead:
     """Draft steps from host memory through the library's host step
     (vt_host_step_*): each call copies the hidden states into the handle's
     pinned staging buffer, launches one CUDA graph (copy in, then the head,
-    whose kernel writes ids and probabilities into pinned host memory),
-    synchronises, and returns host
-    tensors (ids [M, k] int32, probs [M, k] float32) that the next call
-    overwrites.  ``W_high``, ``t2f``, ``k``, M and the options (bias,
+    whose kernel writes ids and probabilities into pinned host memory, then
+    a kernel that publishes the step's sequence number there), waits for
+    that number, and returns host tensors (ids [M, k] int32, probs [M, k]
+    float32) that the next call overwrites.  ``W_high``, ``t2f``, ``k``, M and the options (bias,
     temperature) are fixed; drawing is not offered (a replayed graph repeats
     its step counter).  Write ``head.H_host`` in place and call ``head()``
     to skip the host copy."""

@@ -12,12 +12,16 @@
 // vt_draft_head_ex, whose last CTA writes ids and probabilities straight into
 // a pinned host buffer (pinned memory is addressable from the device, so no
 // copy node follows).  A last small kernel, a programmatic dependent of the
-// head (its launch overlaps the head), waits for the head to complete and
-// moves the head's device error word into the same pinned buffer, clearing
-// it.  Each step is then a host copy of H into the staging buffer, one graph
-// launch, one synchronise (which also makes the kernels' host writes
-// visible), a look at the error word and a host copy out.
+// head (its launch overlaps the head), waits for the head to complete,
+// moves the head's device error word into the same pinned buffer (clearing
+// it), and then, after a system-scope fence, writes the step's sequence
+// number there too.  Each step is then a host copy of H into the staging
+// buffer, one graph launch, a host wait for that sequence number (a spin on
+// the pinned word, which returns ~2.5 us sooner than a stream synchronise;
+// a synchronise takes over if the spin runs long, and reports any launch or
+// kernel error), a look at the error word and a host copy out.
 // The pages have no counterpart: it serves the end-to-end use of the head.
+#include <atomic>
 #include <cstring>
 #include <new>
 
@@ -30,9 +34,12 @@ struct vt_host_step {
   uint16_t* H_pinned = nullptr;   // host, pinned [M, d]
   int32_t* out_pinned = nullptr;  // host, pinned [2, M, k] (ids, prob bits),
                                   // written by the head's kernel, then the
-                                  // head's error word
+                                  // head's error word and the step's
+                                  // sequence number
   uint16_t* H_dev = nullptr;      // device [M, d]
-  void* ws = nullptr;             // device head workspace
+  void* ws = nullptr;             // device head workspace, then the step
+                                  // counter (uint32, after wbytes)
+  unsigned seq = 0;               // steps published so far
 };
 
 namespace {
@@ -50,15 +57,24 @@ __global__ void __launch_bounds__(kCopyThreads)
     dst[i] = src[i];
 }
 
-// *err_out = *err; *err = 0, once the head before it has completed
-// (err_out in pinned host memory: a plain store, read after the step's
-// synchronise).
-__global__ void host_err_publish_kernel(unsigned* err, unsigned* err_out) {
+// Once the head before it has completed: err_out[0] = *err, *err = 0, then
+// the step counter's next value into err_out[1] behind a system-scope
+// fence, so a host that reads that value also sees the head's ids and
+// probabilities and the error word (err_out in pinned host memory).
+__global__ void host_err_publish_kernel(unsigned* err, unsigned* err_out, unsigned* seq) {
   vt::grid_dependency_wait();
   const unsigned e = *err;
-  *err_out = e;
+  err_out[0] = e;
   if (e) *err = 0u;
+  const unsigned n = *seq + 1u;
+  *seq = n;
+  __threadfence_system();
+  *reinterpret_cast<volatile unsigned*>(err_out + 1) = n;
 }
+
+// Host spins on the step's sequence number before a synchronise takes over
+// (about 10-50 ms of polling).
+constexpr long kSpinLimit = 20000000L;
 
 void destroy(vt_host_step* h) {
   if (!h) return;
@@ -93,7 +109,7 @@ extern "C" vt_status vt_host_step_create(const uint16_t* W_high, int32_t V_high,
   h->M = M;
   h->d = d;
   h->k = k;
-  const size_t hbytes = (size_t)M * d * 2, obytes = (size_t)M * k * 8 + 4;
+  const size_t hbytes = (size_t)M * d * 2, obytes = (size_t)M * k * 8 + 8;
   const size_t wbytes = vt_draft_head_workspace_size(M, V_high, k);
   auto bad = [&](const char* what) {
     const cudaError_t e = cudaGetLastError();
@@ -106,10 +122,12 @@ extern "C" vt_status vt_host_step_create(const uint16_t* W_high, int32_t V_high,
   if (cudaMallocHost(&h->H_pinned, hbytes) != cudaSuccess ||
       cudaMallocHost(&h->out_pinned, obytes) != cudaSuccess ||
       cudaMalloc(&h->H_dev, hbytes) != cudaSuccess ||
-      cudaMalloc(&h->ws, wbytes) != cudaSuccess)
+      cudaMalloc(&h->ws, wbytes + 256) != cudaSuccess)
     return bad("allocation");
   std::memset(h->H_pinned, 0, hbytes);
-  if (cudaMemsetAsync(h->ws, 0, wbytes, h->stream) != cudaSuccess) return bad("memset");
+  std::memset(h->out_pinned, 0, obytes);
+  if (cudaMemsetAsync(h->ws, 0, wbytes + 256, h->stream) != cudaSuccess) return bad("memset");
+  unsigned* seq_dev = reinterpret_cast<unsigned*>(static_cast<char*>(h->ws) + wbytes);
   // the device address of the pinned output buffer (the same pointer under
   // unified addressing)
   int32_t* out_devp = nullptr;
@@ -138,7 +156,7 @@ extern "C" vt_status vt_host_step_create(const uint16_t* W_high, int32_t V_high,
     if (st == VT_OK) {
       const cudaError_t pe = launch_dependent(host_err_publish_kernel, dim3(1),
                                               dim3(1), 0, h->stream, err_dev,
-                                              err_out);
+                                              err_out, seq_dev);
       if (pe != cudaSuccess) {
         cudaGetLastError();
         st = fail(VT_ERR_CUDA, std::string("host_err_publish_kernel: ") +
@@ -154,8 +172,10 @@ extern "C" vt_status vt_host_step_create(const uint16_t* W_high, int32_t V_high,
       destroy(h);
       return st;
     }
-    if (pass == 0 && cudaStreamSynchronize(h->stream) != cudaSuccess)
-      return bad("first step");
+    if (pass == 0) {
+      if (cudaStreamSynchronize(h->stream) != cudaSuccess) return bad("first step");
+      h->seq = 1;  // the eager step published 1
+    }
   }
   cudaGraph_t graph = nullptr;
   if (cudaStreamEndCapture(h->stream, &graph) != cudaSuccess || !graph)
@@ -175,10 +195,23 @@ extern "C" vt_status vt_host_step_run(vt_host_step* h, const uint16_t* H_host,
   const size_t mk = (size_t)h->M * h->k;
   if (H_host != h->H_pinned)
     std::memcpy(h->H_pinned, H_host, (size_t)h->M * h->d * 2);
-  if (cudaGraphLaunch(h->exec, h->stream) != cudaSuccess ||
-      cudaStreamSynchronize(h->stream) != cudaSuccess)
+  if (cudaGraphLaunch(h->exec, h->stream) != cudaSuccess)
     return fail(VT_ERR_CUDA, std::string("vt_host_step_run: ") +
                                  cudaGetErrorString(cudaGetLastError()));
+  const unsigned want = ++h->seq;
+  volatile unsigned* published = reinterpret_cast<volatile unsigned*>(h->out_pinned + 2 * mk + 1);
+  for (long spins = 0; *published != want;) {
+    if (++spins > kSpinLimit) {
+      // a long step (a busy GPU) or a failed one: wait for the stream
+      if (cudaStreamSynchronize(h->stream) != cudaSuccess)
+        return fail(VT_ERR_CUDA, std::string("vt_host_step_run: ") +
+                                     cudaGetErrorString(cudaGetLastError()));
+      if (*published != want)
+        return fail(VT_ERR_CUDA, "vt_host_step_run: the step did not publish its result");
+      break;
+    }
+  }
+  std::atomic_thread_fence(std::memory_order_acquire);
   const unsigned err = reinterpret_cast<volatile unsigned*>(h->out_pinned)[2 * mk];
   if (err != 0)
     return fail(VT_ERR_TIMEOUT,

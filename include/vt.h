@@ -419,12 +419,16 @@ vt_status vt_selftest_wait_timeout(uint32_t* err_word, int64_t budget_cycles,
  *     This call allocates and synchronises; the run call does neither.
  *   vt_host_step_run: copies H_host (host, bf16 [M, d]; skipped when it is
  *     the staging buffer) into the staging buffer, launches the graph,
- *     synchronises the handle's stream and writes ids_host [M, k] and
- *     probs_host [M, k] (host).  The graph ends with a small kernel that
- *     moves the head's error word (byte 128 of the handle's workspace) into
- *     the pinned output buffer and clears it: if a bounded wait inside the
- *     head gave up, the call returns VT_ERR_TIMEOUT and writes nothing.
- *     Not thread-safe per handle.
+ *     waits for the step and writes ids_host [M, k] and probs_host [M, k]
+ *     (host).  The graph ends with a small kernel that moves the head's
+ *     error word (byte 128 of the handle's workspace) into the pinned output
+ *     buffer, clears it, and then publishes the step's sequence number there
+ *     behind a system-scope fence; the call waits by polling that number
+ *     (a stream synchronise takes over after ~10-50 ms, and its error, if
+ *     any, is returned as VT_ERR_CUDA).  The graph's last kernel may still
+ *     be exiting when the call returns; the next run queues behind it.  If a
+ *     bounded wait inside the head gave up, the call returns VT_ERR_TIMEOUT
+ *     and writes nothing.  Not thread-safe per handle.
  *   vt_host_step_staging: the pinned [M, d] staging buffer (write H there to
  *     skip the host copy).
  *   vt_host_step_error_word: the device address of the handle's error word

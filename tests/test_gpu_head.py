@@ -179,19 +179,23 @@ def test_tree_draft_m60_every_row():
 
 def test_host_draft_head_graph_steps():
     """HostDraftHead: each call copies new host hidden states in, replays
-    the captured step and returns the same ids and probabilities as a direct
-    device call on those hidden states (both head paths)."""
+    the captured step, waits for the step's published sequence number and
+    returns the same ids and probabilities as a direct device call on those
+    hidden states (both head paths, 40 steps over four inputs)."""
     dev = need_cuda()
     W = synth.normal_bf16((20000, 1024), 0.02, seed=81, device=dev)
     t2f = synth.rank_permutation(40000, 82)[:20000].to(dev)
     for M in (1, 6):
         head = vt.HostDraftHead(W, t2f, 10, M)
-        for step in range(3):
-            H = synth.normal_bf16((M, 1024), 1.0, seed=83 + step + 10 * M)
-            ids_h, probs_h = head(H)
-            ids_d, probs_d = vt.draft_head(H.to(dev), W, t2f, 10)
-            assert torch.equal(ids_h, ids_d.cpu())
-            torch.testing.assert_close(probs_h, probs_d.cpu(), rtol=1e-6, atol=1e-7)
+        Hs = [synth.normal_bf16((M, 1024), 1.0, seed=83 + j + 10 * M) for j in range(4)]
+        refs = [vt.draft_head(H.to(dev), W, t2f, 10) for H in Hs]
+        # consecutive steps on different inputs: a step that returned before
+        # its results landed would show the previous step's ids
+        for step in range(40):
+            j = (3 * step) % 4
+            ids_h, probs_h = head(Hs[j])
+            assert torch.equal(ids_h, refs[j][0].cpu()), step
+            torch.testing.assert_close(probs_h, refs[j][1].cpu(), rtol=1e-6, atol=1e-7)
 
 
 @pytest.mark.parametrize("M", [1, 4])
