@@ -23,6 +23,7 @@ L2, and three copies rotate so no call finds its rows in L2.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -496,6 +497,41 @@ def run_ours(args, world, rank, local):
     sample_per_call = max_over_ranks(sample_secs, world) / sample_steps
     sample_bytes = V_high * d * 2 + M * d * 2 + M * 8
 
+    # ---- the same step with a kept-row bias and temperature 0.8
+    b_high = torch.randn(V_high, device=dev) * 0.1
+
+    def bias_step(i):
+        vt.draft_head(H, W_highs[i % n_copies], t2f, k, out_ids=ids,
+                      out_probs=probs, ws=ws, bias=b_high, temperature=0.8)
+
+    bias_steps = min(args.steps, 5000)
+    bias_secs, _ = time_graph(torch, bias_step, bias_steps,
+                              max(3, args.warmup // 4))
+    bias_per_call = max_over_ranks(bias_secs, world) / bias_steps
+    bias_bytes = alg_bytes + V_high * 4
+
+    # ---- per-request vocabulary sets: four hidden states over two sets of
+    # V_high kept rows (each set's weights are read once per call)
+    sets_rows = [0, 1, 0, 1]
+    Hs = synth.normal_bf16((len(sets_rows), d), 1.0, seed=cfg.seed + 2, device=dev)
+    ids_s = torch.empty(len(sets_rows), k, dtype=torch.int32, device=dev)
+    probs_s = torch.empty(len(sets_rows), k, dtype=torch.float32, device=dev)
+    ws_s = torch.zeros(vt.load().vt_draft_head_sets_workspace_size(
+        len(sets_rows), d, k, 2, (ctypes.c_int32 * 2)(V_high, V_high)),
+        dtype=torch.uint8, device=dev)
+
+    def sets_step(i):
+        j = i % n_copies
+        vt.draft_head_sets(Hs, sets_rows, [W_highs[j], W_highs[(j + 1) % n_copies]],
+                           [t2f, t2f], k, out_ids=ids_s, out_probs=probs_s,
+                           ws=ws_s)
+
+    sets_steps = min(args.steps, 2000)
+    sets_secs, _ = time_graph(torch, sets_step, sets_steps,
+                              max(3, args.warmup // 4))
+    sets_per_call = max_over_ranks(sets_secs, world) / sets_steps
+    sets_bytes = 2 * V_high * d * 2 + len(sets_rows) * (d * 2 + k * 8)
+
     # ---- the full-vocabulary draft distribution q (verification input)
     f2t = torch.full((V,), -1, dtype=torch.int32, device=dev)
     f2t[t2f.long()] = torch.arange(V_high, dtype=torch.int32, device=dev)
@@ -558,6 +594,22 @@ def run_ours(args, world, rank, local):
         },
         "draft_q": dict(q_out, note="q[M, 128256] from [M, 32768] logits; "
                         "bytes = q write + f2t + logits read twice (L2)"),
+        "bias": {
+            "mode": "kept-row bias added to every logit, temperature 0.8, "
+                    "same workload",
+            "us_per_call": bias_per_call * 1e6,
+            "achieved_gbs": bias_bytes / bias_per_call / 1e9,
+            "frac": bias_bytes / bias_per_call / 1e9 / peak,
+        },
+        "vocab_sets": {
+            "mode": "M = 4 hidden states over two kept sets of 32768 rows "
+                    "(rows 0, 2 and 1, 3), d = 4096, k = 10: one row "
+                    "gather, the head per set (tensor-core path at 2 rows), "
+                    "one scatter",
+            "us_per_call": sets_per_call * 1e6,
+            "achieved_gbs": sets_bytes / sets_per_call / 1e9,
+            "frac": sets_bytes / sets_per_call / 1e9 / peak,
+        },
         "full_vocab": {
             "V": V, "us_per_call": full_per_call * 1e6,
             "calls_per_s": 1.0 / full_per_call,

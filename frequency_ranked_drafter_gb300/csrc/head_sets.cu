@@ -10,11 +10,15 @@
 // set s_m exactly as vt_draft_head_ex scores it alone, and when drawing its
 // noise index is still its row m in this call.
 //
-// Rows are grouped by set on the host; for each set used, one small kernel
-// gathers its rows' hidden states into contiguous memory (and writes their
-// row numbers for the noise), the head runs on them (GEMV for one row, the
-// tensor-core path for more), and a second small kernel scatters their ids
-// and probabilities back to their rows.
+// Rows are grouped by set on the host.  One small kernel gathers every
+// row's hidden state into contiguous memory, set by set (and writes the row
+// numbers for the noise); then, for each set used, the head runs on that
+// set's rows (GEMV for one row, the tensor-core path for more), each head a
+// programmatic dependent of the one before (its weights start streaming
+// while the previous set's selection finishes); a last small kernel
+// scatters all ids and probabilities back to their rows.  (With a gather and
+// a scatter around each set's head, two sets of 32768 rows at M = 4 took
+// 107.6 us.)
 #include <vector>
 
 #include "head_common.cuh"
@@ -131,15 +135,21 @@ extern "C" vt_status vt_draft_head_sets(
   float* probs_g = reinterpret_cast<float*>(w + L.probs);
   int32_t* row_ids = reinterpret_cast<int32_t*>(w + L.rows);
   cudaStream_t st = (cudaStream_t)stream;
+  // all rows, set by set: set s's rows sit at [first[s], first[s] + n_s)
+  RowList rl;
+  rl.n = M;
+  std::vector<int> first(S, 0);
+  for (int s = 0, j = 0; s < S; ++s) {
+    first[s] = j;
+    for (int32_t m : rows[s]) rl.rows[j++] = m;
+  }
+  sets_gather_kernel<<<M, 128, 0, st>>>(H, ldh, d, rl, Hg, row_ids);
+  vt_status r = launch_status("sets_gather_kernel");
+  if (r != VT_OK) return r;
   for (int s = 0; s < S; ++s) {
     const int n = (int)rows[s].size();
     if (n == 0) continue;
-    RowList rl;
-    rl.n = n;
-    for (int j = 0; j < n; ++j) rl.rows[j] = rows[s][j];
-    sets_gather_kernel<<<n, 128, 0, st>>>(H, ldh, d, rl, Hg, row_ids);
-    vt_status r = launch_status("sets_gather_kernel");
-    if (r != VT_OK) return r;
+    const int j0 = first[s];
     vt_head_options o;
     if (opts) {
       o = *opts;
@@ -151,13 +161,12 @@ extern "C" vt_status vt_draft_head_sets(
       o.offset = 0;
     }
     o.bias_high = bias_sets ? bias_sets[s] : nullptr;
-    r = draft_head_rows(Hg, n, d, d, W_high_sets[s], V_high_sets[s],
-                        t2f_sets ? t2f_sets[s] : nullptr, k, &o, row_ids,
-                        ids_g, probs_g, w + L.head, L.Hg, stream);
-    if (r != VT_OK) return r;
-    sets_scatter_kernel<<<1, 256, 0, st>>>(ids_g, probs_g, rl, k, out_ids, out_probs);
-    r = launch_status("sets_scatter_kernel");
+    r = draft_head_rows(Hg + (size_t)j0 * d, n, d, d, W_high_sets[s], V_high_sets[s],
+                        t2f_sets ? t2f_sets[s] : nullptr, k, &o, row_ids + j0,
+                        ids_g + (size_t)j0 * k, probs_g + (size_t)j0 * k, w + L.head,
+                        L.Hg, stream);
     if (r != VT_OK) return r;
   }
-  return VT_OK;
+  sets_scatter_kernel<<<1, 256, 0, st>>>(ids_g, probs_g, rl, k, out_ids, out_probs);
+  return launch_status("sets_scatter_kernel");
 }
