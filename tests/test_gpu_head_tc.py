@@ -65,6 +65,8 @@ def test_tc_shapes(d, V_high, M, k):
     (4096, 9728, 60, 10),    # 76 tiles on 152 SMs: the largest split grid
     (2056, 257, 64, 32),     # one full tile and one row, N = 64
     (8200, 640, 3, 4),       # long K, N = 16
+    (1024, 3000, 200, 10),   # N = 208: several 16-column chunks per epilogue warp
+    (512, 2000, 256, 5),     # N = 256: the widest exchange buffer
 ])
 def test_tc_k_split_between_cluster_pairs(d, V_high, M, k):
     """With at most half as many 128-row tiles as SMs (and at least eight K
