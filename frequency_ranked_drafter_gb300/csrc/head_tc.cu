@@ -988,7 +988,11 @@ vt_status head_tc(const uint16_t* H, int M, int d, int64_t ldh,
       !make_map(&tmH, H, (uint64_t)M, (uint64_t)d, (uint64_t)ldh, (uint32_t)a.N))
     return fail(VT_ERR_CUDA, "head_tc: cuTensorMapEncodeTiled failed");
   if (!allow_max_smem(head_tc_gemm_kernel, di)) return VT_ERR_CUDA;
-  const int grid = a.ksplit ? 2 * ntiles : std::min(ntiles, di.num_sms);
+  // Whole tiles: as many waves of tiles as the SMs need, spread evenly
+  // (256 tiles on 152 SMs: 128 CTAs of two tiles rather than 104 of two and
+  // 48 of one, so no SM streams alone at the end; 512 tiles: 128 of four).
+  const int waves = (ntiles + di.num_sms - 1) / di.num_sms;
+  const int grid = a.ksplit ? 2 * ntiles : (ntiles + waves - 1) / waves;
   const int smem = a.stages * stage_bytes + xbytes + 1024;
   // a programmatic dependent of the work ahead of it in the stream; with the
   // K split, in clusters of two CTAs
