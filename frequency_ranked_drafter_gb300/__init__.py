@@ -514,6 +514,11 @@ class HostDraftHead:
         self.ids = torch.empty(M, k, dtype=torch.int32)
         self.probs = torch.empty(M, k, dtype=torch.float32)
         self._lib = lib
+        # per-step call: the entry point and the output pointers, looked up once
+        self._run = lib.vt_host_step_run
+        self._shape = (M, d)
+        self._staging = staging
+        self._out = (self.ids.data_ptr(), self.probs.data_ptr())
 
     @property
     def error_word(self) -> int:
@@ -522,9 +527,18 @@ class HostDraftHead:
         return self._lib.vt_host_step_error_word(self._h)
 
     def __call__(self, H_host: torch.Tensor | None = None):
-        src = self.H_host if H_host is None else H_host.contiguous()
-        _check("vt_host_step_run", self._lib.vt_host_step_run(
-            self._h, src.data_ptr(), self.ids.data_ptr(), self.probs.data_ptr()))
+        if H_host is None:
+            src = self._staging
+        else:
+            if (H_host.dtype != torch.bfloat16 or H_host.is_cuda
+                    or tuple(H_host.shape) != self._shape):
+                raise TypeError(f"H_host must be a host bf16 tensor of shape {self._shape}")
+            if not H_host.is_contiguous():
+                H_host = H_host.contiguous()  # (kept alive through the call)
+            src = H_host.data_ptr()
+        status = self._run(self._h, src, *self._out)
+        if status != VT_OK:
+            _check("vt_host_step_run", status)
         return self.ids, self.probs
 
     def __del__(self):

@@ -196,6 +196,13 @@ def test_host_draft_head_graph_steps():
             ids_h, probs_h = head(Hs[j])
             assert torch.equal(ids_h, refs[j][0].cpu()), step
             torch.testing.assert_close(probs_h, refs[j][1].cpu(), rtol=1e-6, atol=1e-7)
+        # a non-contiguous host view of the same values
+        ids_h, _ = head(Hs[1].t().contiguous().t())
+        assert torch.equal(ids_h, refs[1][0].cpu())
+        with pytest.raises(TypeError):
+            head(torch.zeros(M + 1, 1024, dtype=torch.bfloat16))
+        with pytest.raises(TypeError):
+            head(Hs[0].float())
 
 
 @pytest.mark.parametrize("M", [1, 4])
