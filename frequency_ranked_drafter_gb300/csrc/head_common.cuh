@@ -153,24 +153,6 @@ __device__ __forceinline__ float block_sum(float v, float* scratch) {
   return r;
 }
 
-template <int NT>
-__device__ __forceinline__ void block_best(float& v, int& i, float* sv,
-                                          int* si) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float v2 = __shfl_xor_sync(~0u, v, o);
-    const int i2 = __shfl_xor_sync(~0u, i, o);
-    if (key_beats(v2, i2, v, i)) { v = v2; i = i2; }
-  }
-  if ((threadIdx.x & 31) == 0) { sv[threadIdx.x >> 5] = v; si[threadIdx.x >> 5] = i; }
-  __syncthreads();
-  v = sv[0];
-  i = si[0];
-  for (int w = 1; w < NT / 32; ++w)
-    if (key_beats(sv[w], si[w], v, i)) { v = sv[w]; i = si[w]; }
-  __syncthreads();
-}
-
 // Order-preserving image of a float in uint32 (larger float -> larger
 // key; -0 and +0 share one key; -inf -> 0x007fffff, so 0 is below every
 // real value).

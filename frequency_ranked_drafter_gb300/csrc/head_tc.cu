@@ -141,19 +141,6 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
 
 
 
-// 16 consecutive 32-bit columns of this warp's 32 TMEM lanes (lane = row).
-__device__ __forceinline__ void tmem_ld_32x32_x16(uint32_t taddr, float (&r)[kTcChunk]) {
-  uint32_t* u = reinterpret_cast<uint32_t*>(r);
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]),
-        "=r"(u[6]), "=r"(u[7]), "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]),
-        "=r"(u[12]), "=r"(u[13]), "=r"(u[14]), "=r"(u[15])
-      : "r"(taddr)
-      : "memory");
-}
-
 __device__ __forceinline__ void record_error(unsigned* err, volatile int* abort) {
   *abort = 1;
   atomicExch(err, (unsigned)VT_ERR_TIMEOUT);
@@ -386,7 +373,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t xb = map_to_rank(tc::smem_u32(xbuf), rank ^ 1u);
         for (int c0 = kTcChunk * part; c0 < a.N; c0 += 4 * kTcChunk) {
           float r[kTcChunk];
-          tmem_ld_32x32_x16(tacc + (uint32_t)c0, r);
+          tc::tmem_ld_32x32_x16(tacc + (uint32_t)c0, r);
           tc::tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < kTcChunk; ++j)
@@ -412,7 +399,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const float b = row < a.V_high && a.bias ? __ldg(a.bias + row) : 0.f;
       for (int c0 = kTcChunk * part; c0 < a.N; c0 += 4 * kTcChunk) {
         float r[kTcChunk];
-        tmem_ld_32x32_x16(tacc + (uint32_t)c0, r);
+        tc::tmem_ld_32x32_x16(tacc + (uint32_t)c0, r);
         tc::tmem_ld_wait();
         if (recv) {
 #pragma unroll
