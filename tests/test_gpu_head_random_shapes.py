@@ -1,0 +1,33 @@
+"""Seeded random shapes through vt_draft_head against the oracle: d any
+multiple of 8, V_high from tens of rows to past the K-split bound, M from
+one (GEMV) to 96 (tensor cores, with and without the K split), k from 1 to
+32, with and without the remap.  Every logit and the top-k of every row are
+checked (run_case in test_gpu_head.py).  The shapes are drawn once from a
+fixed seed, so a failure names a reproducible case."""
+import numpy as np
+import pytest
+
+from test_gpu_head import run_case
+
+pytestmark = pytest.mark.gpu
+
+
+def _shapes(n=28, seed=20261202):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        M = int(rng.choice([1, 1, 2, 3, 4, 5, 7, 9, 16, 17, 31, 33, 48, 60, 64, 65, 96]))
+        d = int(rng.integers(1, 513)) * 8
+        # rows: mostly below the K-split bound (76 tiles of 128), some above
+        V_high = int(rng.integers(32, 9728) if i % 4 else rng.integers(9729, 16000))
+        # keep the oracle's work (M * V_high * d multiply-adds) modest
+        while M * V_high * d > 4e8:
+            d = max(8, (d // 2) // 8 * 8)
+        k = int(rng.integers(1, min(32, V_high) + 1))
+        out.append((d, V_high, M, k, bool(rng.integers(0, 2)), 1000 + i))
+    return out
+
+
+@pytest.mark.parametrize("d,V_high,M,k,use_t2f,seed", _shapes())
+def test_random_shape(d, V_high, M, k, use_t2f, seed):
+    run_case(d, V_high, M, k, seed=seed, use_t2f=use_t2f)
