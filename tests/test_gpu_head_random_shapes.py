@@ -2,12 +2,15 @@
 multiple of 8, V_high from tens of rows to past the K-split bound, M from
 one (GEMV) to 96 (tensor cores, with and without the K split), k from 1 to
 32, with and without the remap.  Every logit and the top-k of every row are
-checked (run_case in test_gpu_head.py).  The shapes are drawn once from a
-fixed seed, so a failure names a reproducible case."""
+checked (run_case in test_gpu_head.py); a second set adds a bias, a
+temperature and Gumbel-max draws at random (run_options in
+test_gpu_head_options.py).  The shapes are drawn once from a fixed seed, so
+a failure names a reproducible case."""
 import numpy as np
 import pytest
 
 from test_gpu_head import run_case
+from test_gpu_head_options import run_options
 
 pytestmark = pytest.mark.gpu
 
@@ -31,3 +34,22 @@ def _shapes(n=28, seed=20261202):
 @pytest.mark.parametrize("d,V_high,M,k,use_t2f,seed", _shapes())
 def test_random_shape(d, V_high, M, k, use_t2f, seed):
     run_case(d, V_high, M, k, seed=seed, use_t2f=use_t2f)
+
+
+def _option_shapes(n=16, seed=20261203):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i, (d, V_high, M, k, use_t2f, _) in enumerate(_shapes(n, seed)):
+        T = float(np.round(rng.uniform(0.5, 1.5), 3))
+        out.append((d, V_high, M, k, use_t2f, T, bool(rng.integers(0, 2)),
+                    bool(rng.integers(0, 2)), int(rng.integers(0, 2**62)),
+                    int(rng.integers(0, 2**40)), 2000 + i))
+    return out
+
+
+@pytest.mark.parametrize("d,V_high,M,k,use_t2f,T,use_bias,sample,gen_seed,offset,seed",
+                         _option_shapes())
+def test_random_options(d, V_high, M, k, use_t2f, T, use_bias, sample, gen_seed,
+                        offset, seed):
+    run_options(d, V_high, M, k, seed, T=T, use_bias=use_bias, sample=sample,
+                gen_seed=gen_seed, offset=offset, use_t2f=use_t2f)
